@@ -1,0 +1,496 @@
+#!/usr/bin/env python3
+"""Benchmark: Kimi-K3 KDA decode input projection on one GB300.
+
+Workload: the full overlapped projection of one TP8 rank -- packed
+[4096 + 136, 7168] bf16 weight (Q/K/V/G rows, then F_A/beta rows) and
+W_fb [1024, 128] -- for token counts M in {1, 2, 4, 8, 16, 32, 64, 128}. Each
+call reads a different layer of a 48-layer weight stack (2.92 GB, far above
+the 129 MB L2) so weight reads come from HBM; x stays resident as in decode.
+
+One step = one replay of a captured CUDA graph per M, each graph holding 48
+projection calls (layers 0..47) = 384 calls. Reported value: mean over the M
+values of the device time per call (us), median-free (total time / calls).
+
+Also reported: per-M us/call, HBM GB/s and roofline fraction (bytes =
+2(MK + NK + MN) summed over the three GEMMs), sequential vs overlapped times,
+the dominant kernel's roofline (Q/K/V/G GEMM timed alone), the CPU oracle on
+the host cores, the end-to-end number through host buffers, SM clocks.
+
+--impl reference times the CPU oracle (the plain double-precision reference)
+on a bounded column sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_LIST = (1, 2, 4, 8, 16, 32, 64, 128)
+K, N_QKVG, N_FAB, N_FA, N_FB = 7168, 4096, 136, 128, 1024
+LAYERS = 48
+METRIC = "KDA proj µs/call and HBM GB/s (% of ~8 TB/s) at M=1..128, bf16, 1×GB300"
+UNIT = "us/call"
+WORKLOAD = ("full overlapped KDA decode projection: packed [4096+136, 7168] bf16 + W_fb [1024,128] "
+            "bf16, QKVG on main stream || F_A/beta->F_B (PDL) on aux stream, graph-replayed, "
+            "48-layer weight stack rotated per call")
+
+
+def call_bytes(M: int) -> int:
+    """Algorithmic bytes of one projection call: 2(MK + NK + MN) per GEMM."""
+    g = lambda m, n, k: 2 * (m * k + n * k + m * n)
+    return g(M, N_QKVG, K) + g(M, N_FAB, K) + g(M, N_FB, N_FA)
+
+
+def call_flops(M: int) -> int:
+    return 2 * M * (N_QKVG * K + N_FAB * K + N_FB * N_FA)
+
+
+def qkvg_bytes(M: int) -> int:
+    return 2 * (M * K + N_QKVG * K + M * N_QKVG)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return (float(d["hbm_gbs"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "measured")
+    except Exception:
+        return 6800.0, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: each rank runs the same workload on its GPU)
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group("gloo")
+    return dist
+
+
+def reduce_max(values, dist):
+    """Element-wise max over ranks (host-side timing reduction, gloo)."""
+    if dist is None:
+        return list(values)
+    import torch
+    t = torch.tensor(list(values), dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        if not shutil.which("nvidia-smi"):
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+             "--format=csv,noheader,nounits", "-lms", "100"],
+            stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        # samples under load: power above the idle floor
+        pmax = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in loaded:
+            for name, v in zip(names, r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": pmax}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def run_ours(args):
+    import torch
+    from decode_projection_gemms_gb300 import binding
+    from decode_projection_gemms_gb300.build import build
+    from decode_projection_gemms_gb300.inputs import gen_kda_layer, gen_x
+
+    ws, rank, local = dist_env()
+    dist = dist_init(ws)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or ws == 1:
+        build()
+    barrier(dist)
+    binding.load()
+    hbm_peak, tc_peak, peak_src = load_peaks()
+    m_list = [m for m in M_LIST if m <= args.max_m]
+    L = args.layers
+
+    # weights: layer 0 from the canonical CPU stream, the rest drawn on the GPU
+    wp_stack = torch.empty((L, N_QKVG + N_FAB, K), dtype=torch.bfloat16, device=dev)
+    wfb_stack = torch.empty((L, N_FB, N_FA), dtype=torch.bfloat16, device=dev)
+    for layer in range(L):
+        wp, wfb = gen_kda_layer(layer, seed=0, device="cpu" if layer == 0 else dev)
+        wp_stack[layer].copy_(wp)
+        wfb_stack[layer].copy_(wfb)
+        del wp, wfb
+    xs = {M: gen_x(M, K, seed=0).to(dev) for M in m_list}
+    outs = {M: (torch.empty((M, N_QKVG), dtype=torch.bfloat16, device=dev),
+                torch.empty((M, N_FAB), dtype=torch.bfloat16, device=dev),
+                torch.empty((M, N_FB), dtype=torch.bfloat16, device=dev)) for M in m_list}
+
+    plan = binding.KdaPlan(K, N_QKVG, N_FAB, N_FB, max_M=max(m_list))
+    main = torch.cuda.Stream(device=dev)
+    aux = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(main):
+        evs = binding.make_events()
+
+    def capture(M, mode, qkvg_only=False):
+        plan.set_overlap(mode)
+        g = torch.cuda.CUDAGraph()
+        oq, of, ob = outs[M]
+        # warm-up outside capture (lazy attribute setup)
+        with torch.cuda.stream(main):
+            if qkvg_only:
+                binding.skinny_gemm(xs[M], wp_stack[0, :N_QKVG], oq,
+                                    cfg=plan.get_config(binding.BRANCH_QKVG, M))
+            else:
+                plan.run(xs[M], wp_stack[0], wfb_stack[0], oq, of, ob, aux_stream=aux, events=evs)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=main):
+            for layer in range(L):
+                if qkvg_only:
+                    binding.skinny_gemm(xs[M], wp_stack[layer, :N_QKVG], oq,
+                                        cfg=plan.get_config(binding.BRANCH_QKVG, M))
+                else:
+                    plan.run(xs[M], wp_stack[layer], wfb_stack[layer], oq, of, ob,
+                             aux_stream=aux, events=evs)
+        plan.set_overlap(-1)
+        return g
+
+    graphs = {M: capture(M, -1) for M in m_list}
+    graphs_seq = {M: capture(M, 0) for M in m_list}
+    graphs_ovl = {M: capture(M, 1) for M in m_list}
+    graphs_q = {M: capture(M, -1, qkvg_only=True) for M in m_list}
+
+    def timed(gs, steps):
+        """Replay each graph once per step; per-M device times (ms) summed.
+        Events bracket every replay on the launching stream; no host sync
+        inside the timed region."""
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in m_list] for _ in range(steps)]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0.record(main)
+        for s in range(steps):
+            for i, M in enumerate(m_list):
+                ev[s][i][0].record(main)
+                gs[M].replay()
+                ev[s][i][1].record(main)
+        e1.record(main)
+        torch.cuda.synchronize()
+        barrier(dist)
+        tot = {M: sum(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(steps))
+               for i, M in enumerate(m_list)}
+        return tot, e0.elapsed_time(e1)
+
+    # warm-up
+    with torch.cuda.stream(main):
+        for _ in range(args.warmup):
+            for M in m_list:
+                graphs[M].replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(main):
+        tot, wall_ms = timed(graphs, args.steps)
+        tot_seq, _ = timed(graphs_seq, args.cmp_steps)
+        tot_ovl, _ = timed(graphs_ovl, args.cmp_steps)
+        tot_q, _ = timed(graphs_q, args.cmp_steps)
+    e2e = run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist)
+    clock_info = clocks.stop()
+
+    # reductions (max over ranks)
+    keys = list(m_list)
+    vals = reduce_max([tot[M] for M in keys] + [tot_seq[M] for M in keys] +
+                      [tot_ovl[M] for M in keys] + [tot_q[M] for M in keys] + [wall_ms], dist)
+    nM = len(keys)
+    tot = dict(zip(keys, vals[0:nM]))
+    tot_seq = dict(zip(keys, vals[nM:2 * nM]))
+    tot_ovl = dict(zip(keys, vals[2 * nM:3 * nM]))
+    tot_q = dict(zip(keys, vals[3 * nM:4 * nM]))
+    wall_ms = vals[4 * nM]
+
+    per_m = {}
+    for M in keys:
+        us = tot[M] * 1e3 / (args.steps * L)
+        us_seq = tot_seq[M] * 1e3 / (args.cmp_steps * L)
+        us_ovl = tot_ovl[M] * 1e3 / (args.cmp_steps * L)
+        us_q = tot_q[M] * 1e3 / (args.cmp_steps * L)
+        roof_us = max(call_bytes(M) / (hbm_peak * 1e3), call_flops(M) / (tc_peak * 1e6))
+        per_m[str(M)] = {
+            "us_per_call": round(us, 3),
+            "gbs": round(call_bytes(M) / (us * 1e3), 1),
+            "roofline_us": round(roof_us, 3),
+            "frac_of_roofline": round(roof_us / us, 4),
+            "frac_of_8tbs": round(call_bytes(M) / (us * 1e3) / 8000.0, 4),
+            "overlap": bool(plan.overlap_at(M)),
+            "us_sequential": round(us_seq, 3),
+            "us_overlapped": round(us_ovl, 3),
+            "overlap_speedup": round(us_seq / us_ovl, 4),
+            "qkvg_kernel_us": round(us_q, 3),
+            "qkvg_kernel_gbs": round(qkvg_bytes(M) / (us_q * 1e3), 1),
+            "configs": {b: plan.get_config(i, M).as_dict()
+                        for i, b in enumerate(("qkvg", "fab", "fb"))},
+        }
+    value = statistics.fmean(per_m[str(M)]["us_per_call"] for M in keys)
+    q_bytes = sum(qkvg_bytes(M) for M in keys)
+    q_time_us = sum(per_m[str(M)]["qkvg_kernel_us"] for M in keys)
+    achieved = q_bytes / (q_time_us * 1e3)  # GB/s
+    cpu = run_cpu_baseline(args) if (rank == 0 and not args.no_cpu) else None
+    plan.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 3),
+            "unit": UNIT,
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(wall_ms / args.steps, 4),
+            "higher_is_better": False,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded; x ~ N(0,1), W ~ N(0, 0.02^2); random weights)",
+            "config": {"workload": WORKLOAD, "M": keys, "K": K, "N_qkvg": N_QKVG,
+                       "N_fab": N_FAB, "N_fb": N_FB, "layers": L,
+                       "weight_stack_gb": round(L * (N_QKVG + N_FAB) * K * 2 / 1e9 +
+                                                L * N_FB * N_FA * 2 / 1e9, 3),
+                       "l2": "inputs larger than L2: weight stack rotated per call",
+                       "value_is": "mean over M of device time per projection call",
+                       "parallelism": f"replicas x{ws}"},
+            "per_m": per_m,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                         "kernel": "Q/K/V/G GEMM (per-M configured kernel), timed alone",
+                         "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * len(keys) * L * 3,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist):
+    """Same metric through the public API with host buffers: every call copies
+    its x from pinned host memory and its three outputs back."""
+    import torch
+    from decode_projection_gemms_gb300.inputs import gen_x
+    L = args.layers
+    hx = {M: gen_x(M, K, seed=M).pin_memory() for M in m_list}
+    dx = {M: torch.empty((M, K), dtype=torch.bfloat16, device=dev) for M in m_list}
+    dout = {M: (torch.empty((M, N_QKVG), dtype=torch.bfloat16, device=dev),
+                torch.empty((M, N_FAB), dtype=torch.bfloat16, device=dev),
+                torch.empty((M, N_FB), dtype=torch.bfloat16, device=dev)) for M in m_list}
+    hout = {M: tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dout[M])
+            for M in m_list}
+    graphs = {}
+    for M in m_list:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(main):
+            dx[M].copy_(hx[M], non_blocking=True)
+            plan.run(dx[M], wp_stack[0], wfb_stack[0], *dout[M], aux_stream=aux, events=evs)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=main):
+            for layer in range(L):
+                dx[M].copy_(hx[M], non_blocking=True)
+                plan.run(dx[M], wp_stack[layer], wfb_stack[layer], *dout[M], aux_stream=aux,
+                         events=evs)
+                for d, h in zip(dout[M], hout[M]):
+                    h.copy_(d, non_blocking=True)
+        graphs[M] = g
+    steps = max(1, args.cmp_steps)
+    tot = {M: 0.0 for M in m_list}
+    with torch.cuda.stream(main):
+        for M in m_list:
+            graphs[M].replay()
+        torch.cuda.synchronize()
+        barrier(dist)
+        for _ in range(steps):
+            for M in m_list:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(main)
+                graphs[M].replay()
+                b.record(main)
+                b.synchronize()
+                tot[M] += a.elapsed_time(b)
+    vals = reduce_max([tot[M] for M in m_list], dist)
+    us = [v * 1e3 / (steps * L) for v in vals]
+    h2d = sum(M * K * 2 for M in m_list) * L
+    d2h = sum(M * (N_QKVG + N_FAB + N_FB) * 2 for M in m_list) * L
+    return {"value": round(statistics.fmean(us), 3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "per_m_us": {str(M): round(u, 3) for M, u in zip(m_list, us)}}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+
+def oracle_step(stride: int, nthreads: int, m_list):
+    """Oracle on a column sample (every `stride`-th output feature of each
+    GEMM); returns host seconds per call, averaged over M, scaled back to the
+    full column count."""
+    import numpy as np
+    import oracle
+    from decode_projection_gemms_gb300.inputs import bf16_bits, gen_kda_layer, gen_x
+    wp, wfb = gen_kda_layer(0, seed=0)
+    wpb, wfbb = bf16_bits(wp), bf16_bits(wfb)
+    wq = np.ascontiguousarray(wpb[:N_QKVG:stride])
+    wf = wpb[N_QKVG:]
+    wfs = np.ascontiguousarray(wfbb[::stride])
+    times = []
+    for M in m_list:
+        xb = bf16_bits(gen_x(M, K, seed=0))
+        t0 = time.perf_counter()
+        oracle.gemm(xb, wq, nthreads)
+        fab = oracle.gemm(xb, wf, nthreads)               # F_A/beta is small: all columns
+        fa = oracle.f64_to_bf16(fab[:, :N_FA])
+        oracle.gemm(fa, wfs, nthreads)
+        dt = time.perf_counter() - t0
+        # scale the sampled Q/K/V/G and F_B parts to all columns
+        frac_sampled = (wq.shape[0] * K + N_FAB * K + wfs.shape[0] * N_FA)
+        frac_full = (N_QKVG * K + N_FAB * K + N_FB * N_FA)
+        times.append(dt * frac_full / frac_sampled)
+    return statistics.fmean(times)
+
+
+def run_cpu_baseline(args):
+    nthreads = os.cpu_count() or 1
+    stride = 1
+    t = oracle_step(stride, nthreads, [m for m in M_LIST if m <= args.max_m])
+    return {"value": round(t * 1e6, 1), "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"double-precision oracle, full projection (all output features), one "
+                      f"call per M in {list(M_LIST)} on layer 0, {nthreads} threads over output "
+                      f"features; mean over M"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    m_list = [m for m in M_LIST if m <= args.max_m]
+    nthreads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle_step(args.cpu_stride * 4, nthreads, m_list[:1])
+    t0 = time.perf_counter()
+    vals = [oracle_step(args.cpu_stride, nthreads, m_list) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    value = statistics.fmean(vals) * 1e6
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(wall * 1e3 / max(1, args.steps), 2),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; x ~ N(0,1), W ~ N(0, 0.02^2))",
+        "config": {"workload": WORKLOAD, "M": m_list, "K": K, "N_qkvg": N_QKVG, "N_fab": N_FAB,
+                   "N_fb": N_FB, "value_is": "mean over M of host time per projection call"},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": nthreads,
+                         "kind": "oracle",
+                         "sample": f"every {args.cpu_stride}th output feature of Q/K/V/G and F_B, "
+                                   "all of F_A/beta, scaled to all columns"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--max-m", type=int, default=128)
+    ap.add_argument("--cmp-steps", type=int, default=20,
+                    help="steps for the sequential/overlapped/kernel-alone comparisons")
+    ap.add_argument("--cpu-stride", type=int, default=16,
+                    help="column sampling stride of the CPU oracle")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,96 @@
+// Host side of the CUDA-core split-K kernel: validation, scratch sizing and
+// launch. The kernel itself is in kp_cc_kernel.cuh.
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "kp_cc_kernel.cuh"
+
+namespace kp {
+
+namespace {
+
+constexpr int kMaxSmem = 200 * 1024;
+
+int cc_variant(int R, int U) {
+    for (int v = 0; v < kCCVariants; ++v)
+        if (kCCR[v] == R && kCCU[v] == U) return v;
+    return -1;
+}
+
+CCKernelFn cc_kernel(int M, int R, int U) {
+    const int v = cc_variant(R, U);
+    if (v < 0 || M < 1 || M > 16) return nullptr;
+    return M <= 8 ? cc_table_lo[M - 1][v] : cc_table_hi[M - 9][v];
+}
+
+// K slice length: ceil(K / S) rounded up to 8 elements (16 bytes).
+int cc_slice(int K, int S) {
+    int ks = (K + S - 1) / S;
+    return (ks + 7) & ~7;
+}
+
+std::mutex g_attr_mu;
+std::set<std::pair<const void *, int>> g_attr_done;  // (kernel, device) raised to kMaxSmem
+
+cudaError_t ensure_smem_attr(const void *fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (g_attr_done.count({fn, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess) g_attr_done.insert({fn, dev});
+    return e;
+}
+
+}  // namespace
+
+bool cc_supported(int M, int K, const kp_cfg &c) {
+    if (M < 1 || M > 16 || K < 8 || (K & 7)) return false;
+    if (c.split_k < 1 || c.split_k > K / 8) return false;
+    if (c.block < 32 || c.block > 256 || (c.block & 31)) return false;
+    if (!cc_kernel(M, c.rows, c.k_unroll)) return false;
+    const int ks = cc_slice(K, c.split_k);
+    return static_cast<long long>(M) * ks * 4 <= kMaxSmem;  // x slice fits in shared memory
+}
+
+Scratch cc_scratch(int M, int N, int K, const kp_cfg &c) {
+    Scratch s;
+    const int ks = cc_slice(K, c.split_k);
+    const int S = (K + ks - 1) / ks;
+    if (S > 1) {
+        const int rows_cta = (c.block / 32) * c.rows;
+        s.floats = static_cast<size_t>(S) * M * N;
+        s.counters = static_cast<size_t>((N + rows_cta - 1) / rows_cta);
+    }
+    return s;
+}
+
+cudaError_t cc_launch(const GemmArgs &a, const kp_cfg &c, cudaStream_t stream) {
+    if (!cc_supported(a.M, a.K, c)) return cudaErrorInvalidValue;
+    CCKernelFn fn = cc_kernel(a.M, c.rows, c.k_unroll);
+    CCParams p;
+    p.a = a;
+    p.Ks = cc_slice(a.K, c.split_k);
+    p.S = (a.K + p.Ks - 1) / p.Ks;
+    p.rows_cta = (c.block / 32) * c.rows;
+    const int tiles = (a.N + p.rows_cta - 1) / p.rows_cta;
+    const size_t smem = static_cast<size_t>(a.M) * p.Ks * sizeof(float);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn));
+    if (e != cudaSuccess) return e;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles, p.S, 1);
+    cfg.blockDim = dim3(c.block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (c.flags & KP_FLAG_PDL) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
+}  // namespace kp

@@ -1,0 +1,211 @@
+/*
+ * kdaproj.h -- C ABI of the GB300 (sm_103a) KDA decode-projection library.
+ *
+ * The operation is the low-M "skinny GEMM"
+ *
+ *     y[m, n] = bf16( sum_k x[m, k] * W[n, k] ),   fp32 accumulation,
+ *
+ * i.e. C[M,N] = A[M,K] * B[N,K]^T with bf16 inputs, fp32 accumulation and bf16
+ * output ("[Model] Kimi K3 support part 1", vllm PR 50089, section
+ * "关键源码片段", CuteSkinnyGemm docstring), applied to the Kimi-K3 KDA input
+ * projections of one TP8 rank ("[Kimi-K3] Overlap low-M TP8 KDA projections",
+ * vllm PR 54697, section "关键源码片段", run_kda_projection_overlap):
+ *
+ *   main stream:  out_qkvg = x * W_packed[0 : N_qkvg]^T            (Q/K/V/G)
+ *   aux stream:   out_fab  = x * W_packed[N_qkvg : N_qkvg+N_fab]^T (F_A/beta)
+ *                 out_fb   = out_fab[:, 0:128] * W_fb^T            (F_B, chained
+ *                            with programmatic dependent launch)
+ *   fork/join:    events[0] recorded on main, waited on by aux; events[1]
+ *                 recorded on aux, waited on by main.
+ *
+ * Layout and ownership (every call):
+ *   - All matrices are bf16, row-major, densely packed (row stride = number of
+ *     columns) except F_B's input, which is the F_A half of out_fab read in
+ *     place with row stride N_fab.
+ *   - Every device pointer must be 16-byte aligned. K must be a multiple of 8
+ *     (16-byte rows). Pointers are device (or managed) memory owned by the
+ *     caller; the library never frees or retains them after the call returns.
+ *   - Streams and events are the caller's CUDA handles (cudaStream_t /
+ *     cudaEvent_t); the library only enqueues work on them. NULL stream = the
+ *     legacy default stream.
+ *   - Calls are asynchronous: they return once the work is enqueued. Outputs
+ *     are valid when the stream's work completes.
+ *
+ * Errors: every function returns an int; 0 (KP_OK) on success, a negative
+ * kp_status otherwise, and kp_last_error() (thread-local) then describes the
+ * failure, including the CUDA runtime's message for KP_ECUDA. Argument errors
+ * are detected before anything is enqueued. Nothing throws across this ABI.
+ * Kernel-side waits are bounded: a wait that runs out records a code that
+ * kp_device_error() returns, and the kernel finishes instead of hanging.
+ *
+ * Determinism: the configuration used for a call depends only on (M, N, K)
+ * and the loaded table (never on stream state), and every split-K reduction
+ * sums its partials in a fixed order, so repeated calls, the sequential and
+ * the overlapped projection, and graph replays give bit-identical outputs.
+ */
+#ifndef KDAPROJ_H
+#define KDAPROJ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same tags as cudaStream_t / cudaEvent_t, so those convert implicitly. */
+typedef struct CUstream_st *kp_stream_t;
+typedef struct CUevent_st *kp_event_t;
+
+#define KDAPROJ_VERSION 1
+
+#if defined(__GNUC__)
+#define KP_API __attribute__((visibility("default")))
+#else
+#define KP_API
+#endif
+
+enum kp_status {
+    KP_OK = 0,
+    KP_EINVAL = -1,   /* NULL pointer or out-of-range argument */
+    KP_EALIGN = -2,   /* a pointer is not 16-byte aligned */
+    KP_ESHAPE = -3,   /* unsupported shape (K % 8 != 0, N < 1, N_fab < 128 ...) */
+    KP_ENOPLAN = -4,  /* NULL plan handle */
+    KP_ECUDA = -5,    /* a CUDA runtime call failed; see kp_last_error() */
+    KP_ETOOBIG = -6,  /* M above the plan's max_M (its workspace would overflow) */
+    KP_ENODEV = -7,   /* current device is not an sm_103 GPU */
+    KP_ECONFIG = -8,  /* explicit kp_cfg invalid for this shape */
+    KP_EIO = -9       /* autotune table file unreadable or malformed */
+};
+
+/* Kernel families. */
+enum kp_kind {
+    KP_KIND_AUTO = 0,  /* look the shape up in the table (or the built-in rule) */
+    KP_KIND_CC = 1,    /* CUDA-core split-K weight-streaming GEMV, M <= 16 */
+    KP_KIND_TC05 = 2,  /* TMA-fed tcgen05/TMEM stream-K tile kernel, any M */
+    KP_KIND_SMALLK = 3 /* CUDA-core small-K kernel (K <= 256), the F_B shape */
+};
+
+enum kp_flags {
+    KP_FLAG_PDL = 1 /* launch with programmatic stream serialisation: the
+                       kernel may start (and stream its weights) while the
+                       previous kernel on the stream finishes; it waits for
+                       that kernel before touching x, y or scratch */
+};
+
+/* One kernel configuration. Fields a kind does not use are ignored. */
+typedef struct kp_cfg {
+    int32_t kind;     /* enum kp_kind */
+    int32_t split_k;  /* CC: number of K slices S >= 1 (S > 1 uses scratch) */
+    int32_t block;    /* CC, SMALLK: threads per CTA (multiple of 32, <= 1024) */
+    int32_t rows;     /* CC: output rows per warp (1, 2, 4, 8);
+                         SMALLK: output rows per CTA (1..64) */
+    int32_t k_unroll; /* CC: 16-byte W loads in flight per row per lane (1, 2, 4) */
+    int32_t ctas;     /* TC05: persistent CTAs (0 = one per SM) */
+    int32_t stages;   /* TC05: shared-memory pipeline stages (0 = as many as fit) */
+    int32_t flags;    /* enum kp_flags */
+} kp_cfg;
+
+/* Opaque plan for the full KDA projection. */
+typedef struct kda_plan kda_plan;
+
+/* ---------------------------------------------------------------------------
+ * skinny_gemm: y[M, N] = bf16(x[M, K] * W[N, K]^T), fp32 accumulation.
+ *   x   device, [M, K] bf16, row-major
+ *   W   device, [N, K] bf16, row-major (K contiguous)
+ *   y   device, [M, N] bf16, row-major; written, never read
+ *   cfg NULL or kind == KP_KIND_AUTO: the autotune table picks the kernel;
+ *       otherwise the given configuration is validated and used.
+ * M == 0 is a no-op. M > 256 is processed in 256-row slices.
+ * Scratch: split-K partial sums and tile counters live in a per-device
+ * workspace owned by the library. It grows on demand, so the first call of a
+ * larger shape may allocate (cudaMalloc); do one call per shape before stream
+ * capture. Calls that use this workspace must not run concurrently on one
+ * device (use one stream, or kda_proj_* whose plans own their scratch).
+ * Returns KP_OK, KP_EINVAL, KP_EALIGN, KP_ESHAPE, KP_ECONFIG, KP_ENODEV,
+ * KP_ECUDA. */
+KP_API int skinny_gemm(const void *x, const void *W, void *y, int M, int N, int K,
+                const kp_cfg *cfg, kp_stream_t stream);
+
+/* Host-only: the configuration skinny_gemm would use for (M, N, K) on a
+ * device with `num_sms` SMs (0 = query the current device). Lookup rounds M
+ * up to the next measured bucket of an (N, K) entry; shapes missing from the
+ * table use the built-in rule. Returns KP_OK or KP_EINVAL. */
+KP_API int kp_select_config(int M, int N, int K, int num_sms, kp_cfg *out);
+
+/* Host-only: load an autotune table (text, see the package's tune/ folder),
+ * replacing the loaded one. Plans made earlier keep their configurations.
+ * Returns KP_OK, KP_EINVAL or KP_EIO. kp_table_clear() drops it. */
+KP_API int kp_table_load(const char *path);
+KP_API int kp_table_clear(void);
+KP_API int kp_table_size(void);
+
+/* ---------------------------------------------------------------------------
+ * kda_proj_plan: prepare the projection for hidden size K, N_qkvg Q/K/V/G
+ * rows, N_fab F_A/beta rows (the first 128 are F_A) and N_fb F_B rows, for
+ * token counts 1..max_M. Picks a configuration per (branch, M) from the table,
+ * and allocates (cudaMalloc, on the current device) the scratch of each branch
+ * separately so the two streams never share it. The plan is immutable after
+ * creation except through kda_proj_set_*; it is not thread-safe to modify a
+ * plan while another thread runs it.
+ * Returns KP_OK, KP_EINVAL, KP_ESHAPE, KP_ENODEV or KP_ECUDA. */
+KP_API int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_plan **out);
+
+/* Overlap mode: -1 = per-M flag from the table (default), 0 = always
+ * sequential on main_stream, 1 = always overlapped (when aux and events are
+ * given). Returns KP_OK, KP_ENOPLAN, KP_EINVAL. */
+KP_API int kda_proj_set_overlap(kda_plan *plan, int mode);
+
+/* Branch ids for kda_proj_get_config / kda_proj_set_config. */
+enum kp_branch { KP_BRANCH_QKVG = 0, KP_BRANCH_FAB = 1, KP_BRANCH_FB = 2 };
+
+/* Read or replace the configuration a plan uses for (branch, M). A replaced
+ * configuration must fit the scratch the plan allocated (else KP_ETOOBIG).
+ * Returns KP_OK, KP_ENOPLAN, KP_EINVAL, KP_ECONFIG, KP_ETOOBIG. */
+KP_API int kda_proj_get_config(const kda_plan *plan, int branch, int M, kp_cfg *out);
+KP_API int kda_proj_set_config(kda_plan *plan, int branch, int M, const kp_cfg *cfg);
+
+/* Whether the plan overlaps at this M (1) or runs sequentially (0). */
+KP_API int kda_proj_overlap_at(const kda_plan *plan, int M);
+
+/* ---------------------------------------------------------------------------
+ * kda_proj_run: the full projection for M tokens (0 <= M <= max_M).
+ *   x         device [M, K] bf16
+ *   W_packed  device [N_qkvg + N_fab, K] bf16, Q/K/V/G rows first
+ *   W_fb      device [N_fb, 128] bf16
+ *   out_qkvg  device [M, N_qkvg] bf16 (written)
+ *   out_fab   device [M, N_fab] bf16 (written; columns 0..127 are F_A, the
+ *             rest beta; F_B reads F_A from here)
+ *   out_fb    device [M, N_fb] bf16 (written)
+ *   main_stream, aux_stream, events[2]: caller-owned. When the plan overlaps
+ *   at this M and aux_stream and events are all non-NULL, the F_A/beta -> F_B
+ *   branch runs on aux_stream, forked from and joined back into main_stream
+ *   with events[0] / events[1]; otherwise all three kernels run in order on
+ *   main_stream. Either way, on return main_stream is ordered after all
+ *   outputs. The sequence allocates nothing and never synchronises, so it can
+ *   be captured into a CUDA graph (capture main_stream; aux joins through
+ *   events[0]).
+ * Returns KP_OK, KP_ENOPLAN, KP_EINVAL, KP_EALIGN, KP_ETOOBIG, KP_ECUDA. */
+KP_API int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, const void *W_fb,
+                 void *out_qkvg, void *out_fab, void *out_fb, int M,
+                 kp_stream_t main_stream, kp_stream_t aux_stream, kp_event_t events[2]);
+
+/* Free the plan's scratch (synchronises the device first). NULL is a no-op. */
+KP_API int kda_proj_destroy(kda_plan *plan);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics. */
+KP_API const char *kp_last_error(void);           /* thread-local, never NULL */
+KP_API int kp_version(void);                       /* KDAPROJ_VERSION */
+/* Reads and clears the device-side error word of the current device: 0 if
+ * no kernel wait has run out, else the code of the first one (synchronous:
+ * it waits for the device). Returns KP_OK or KP_ECUDA. */
+KP_API int kp_device_error(int *code);
+/* Bytes of scratch a configuration needs for (M, N, K), for tests/tools. */
+KP_API int kp_scratch_bytes(int M, int N, int K, const kp_cfg *cfg, int num_sms, size_t *bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDAPROJ_H */

@@ -1,0 +1,147 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every function
+``include/kdaproj.h`` declares, and its host-only logic (argument checks,
+autotune-table parsing, configuration selection, scratch sizing) works."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from decode_projection_gemms_gb300 import binding
+from decode_projection_gemms_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kdaproj.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^KP_API\s+(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("skinny_gemm", "kda_proj_plan", "kda_proj_run", "kda_proj_destroy",
+                     "kp_last_error"):
+        assert required in names
+    assert set(names) == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, f"{name} not exported"
+        getattr(lib, name)
+    # internal symbols stay hidden
+    assert not any(s.startswith("_ZN2kp") for s in exported)
+
+
+def test_version_and_error_string(lib):
+    assert lib.kp_version() == 1
+    assert isinstance(lib.kp_last_error(), bytes)
+
+
+def test_argument_errors_need_no_device(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.skinny_gemm(p, p, p, 1, 8, 12, None, None) == binding.KP_ESHAPE     # K % 8
+    assert b"multiple of 8" in lib.kp_last_error()
+    assert lib.skinny_gemm(p, p, p, -1, 8, 16, None, None) == binding.KP_EINVAL
+    assert lib.skinny_gemm(p, p, p, 0, 8, 16, None, None) == binding.KP_OK         # M = 0: no-op
+    assert lib.skinny_gemm(None, p, p, 1, 8, 16, None, None) == binding.KP_EINVAL
+    q = ctypes.c_void_p(24)
+    assert lib.skinny_gemm(q, p, p, 1, 8, 16, None, None) == binding.KP_EALIGN
+    assert lib.kda_proj_run(None, p, p, p, p, p, p, 1, None, None, None) == binding.KP_ENOPLAN
+    out = ctypes.c_void_p()
+    assert lib.kda_proj_plan(7168, 4096, 100, 1024, 16, ctypes.byref(out)) == binding.KP_ESHAPE
+    assert lib.kda_proj_plan(7170, 4096, 136, 1024, 16, ctypes.byref(out)) == binding.KP_ESHAPE
+    assert lib.kda_proj_plan(7168, 4096, 136, 1024, 0, ctypes.byref(out)) == binding.KP_EINVAL
+    assert lib.kda_proj_destroy(None) == binding.KP_OK
+    assert lib.kda_proj_set_overlap(None, 0) == binding.KP_ENOPLAN
+
+
+def test_builtin_rule(lib):
+    binding.table_clear()
+    try:
+        c = binding.select_config(1, 4096, 7168, num_sms=152)
+        assert c.kind == binding.KIND_CC and c.split_k >= 1
+        c = binding.select_config(64, 4096, 7168, num_sms=152)
+        assert c.kind == binding.KIND_TC05
+        c = binding.select_config(8, 1024, 128, num_sms=152)
+        assert c.kind == binding.KIND_SMALLK
+    finally:
+        binding.table_load()
+
+
+def test_table_lookup_rounds_m_up(lib, tmp_path):
+    t = tmp_path / "t.txt"
+    t.write_text(
+        "# M N K kind split_k block rows k_unroll ctas stages flags overlap\n"
+        "1 4096 7168 cc 7 256 4 2 0 0 1 1\n"
+        "4 4096 7168 cc 5 128 2 4 0 0 1 1  # trailing comment\n"
+        "16 4096 7168 tc05 1 0 0 0 148 6 1 0\n"
+        "64 4096 7168 tc05 1 0 0 0 152 4 0 1\n")
+    binding.table_load(str(t))
+    try:
+        assert binding.table_size() == 4
+        c = binding.select_config(1, 4096, 7168, 152)
+        assert (c.kind, c.split_k, c.block, c.rows, c.k_unroll) == (binding.KIND_CC, 7, 256, 4, 2)
+        for M in (2, 3, 4):
+            c = binding.select_config(M, 4096, 7168, 152)
+            assert (c.kind, c.split_k, c.block, c.rows) == (binding.KIND_CC, 5, 128, 2)
+        for M in (5, 9, 16):
+            c = binding.select_config(M, 4096, 7168, 152)
+            assert (c.kind, c.ctas, c.stages) == (binding.KIND_TC05, 148, 6)
+        c = binding.select_config(33, 4096, 7168, 152)
+        assert (c.kind, c.ctas, c.stages, c.flags) == (binding.KIND_TC05, 152, 4, 0)
+        # beyond the largest bucket, or another (N, K): built-in rule
+        c = binding.select_config(100, 4096, 7168, 152)
+        assert c.kind == binding.KIND_TC05 and c.ctas == 0
+        c = binding.select_config(1, 4096, 1024, 152)
+        assert c.kind == binding.KIND_CC
+    finally:
+        binding.table_load()
+
+
+def test_table_rejects_malformed(lib, tmp_path):
+    t = tmp_path / "bad.txt"
+    t.write_text("1 4096 7168 cc 7 256\n")
+    with pytest.raises(binding.KdaProjError) as e:
+        binding.table_load(str(t))
+    assert e.value.code == binding.KP_EIO
+    with pytest.raises(binding.KdaProjError):
+        binding.table_load(str(tmp_path / "missing.txt"))
+    binding.table_load()
+
+
+def test_scratch_sizes(lib):
+    cc = binding.KpCfg.make("cc", split_k=7, block=256, rows=4, k_unroll=2)
+    # S x M x N fp32 partials + one counter per 32-row tile
+    assert binding.scratch_bytes(4, 4096, 7168, cc, 152) == 7 * 4 * 4096 * 4 + (4096 // 32) * 4
+    one = binding.KpCfg.make("cc", split_k=1, block=256, rows=4, k_unroll=2)
+    assert binding.scratch_bytes(4, 4096, 7168, one, 152) == 0
+    tc = binding.KpCfg.make("tc05", ctas=152, stages=4)
+    # G x 2 partial tiles of Mpad x 128 fp32 + one counter per 128-row tile
+    assert binding.scratch_bytes(20, 4096, 7168, tc, 152) == 152 * 2 * 32 * 128 * 4 + 32 * 4
+    bad = binding.KpCfg.make("cc", split_k=1, block=256, rows=8, k_unroll=1)
+    with pytest.raises(binding.KdaProjError) as e:
+        binding.scratch_bytes(16, 4096, 7168, bad, 152)     # 8 x 16 accumulators: not built
+    assert e.value.code == binding.KP_ECONFIG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = binding._lib
+    binding._lib = None
+    try:
+        with pytest.raises(ImportError):
+            binding.load(str(tmp_path / "nope.so"))
+    finally:
+        binding._lib = saved

@@ -1,0 +1,320 @@
+"""CUDA path vs the CPU oracle, element by element, on the same seeded inputs.
+
+Tolerance (bf16 output, fp32 accumulation): |gpu - ref| <= 4 ulp_bf16(|ref|)
++ 1e-3 per element; outputs are NaN-poisoned before each call so an element a
+kernel never writes fails. F_B's bound adds the propagated F_A tolerance
+(sum_k dF_A[k] |W_fb[n, k]|), which is zero extra whenever F_A matches.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from decode_projection_gemms_gb300 import binding
+from decode_projection_gemms_gb300.binding import KpCfg
+from decode_projection_gemms_gb300.inputs import bf16_bits, gen_w, gen_x
+
+from gpu_helpers import check_gemm, check_kda, gemm_case, kda_inputs, poisoned, to_f64
+
+pytestmark = pytest.mark.gpu
+
+CC_VARIANTS = [(1, 4), (2, 2), (2, 4), (4, 1), (4, 2), (8, 1)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from decode_projection_gemms_gb300.build import build
+    build()
+    binding.load()
+    yield
+    assert binding.device_error() == 0
+
+
+# ---- single skinny GEMM: M=1, K=2048, N=1024, x ~ U(-1, 1), seed 0 -------------------
+
+def config1():
+    return gemm_case(1, 1024, 2048, seed=0, dist="uniform")
+
+
+def test_config1_auto():
+    x, W = config1()
+    check_gemm(x, W, None, "auto")
+
+
+@pytest.mark.parametrize("R,U", CC_VARIANTS)
+@pytest.mark.parametrize("S", [1, 3, 8])
+def test_config1_cc(R, U, S):
+    x, W = config1()
+    check_gemm(x, W, KpCfg.make("cc", split_k=S, block=256, rows=R, k_unroll=U), "cc")
+
+
+@pytest.mark.parametrize("ctas,stages", [(0, 0), (37, 2), (152, 4), (5, 3)])
+def test_config1_tc05(ctas, stages):
+    x, W = config1()
+    check_gemm(x, W, KpCfg.make("tc05", ctas=ctas, stages=stages), "tc05")
+
+
+# ---- CUDA-core kernel: every M bucket, ragged N, several K -------------------------------
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 11, 16])
+@pytest.mark.parametrize("N,K", [(136, 7168), (1000, 1024), (4096, 1032)])
+def test_cc_shapes(M, N, K):
+    x, W = gemm_case(M, N, K, seed=M)
+    for R, U in CC_VARIANTS:
+        cfg = KpCfg.make("cc", split_k=5, block=256, rows=R, k_unroll=U)
+        try:
+            binding.scratch_bytes(M, N, K, cfg, 152)
+        except binding.KdaProjError:
+            continue  # variant not built for this M
+        check_gemm(x, W, cfg, "cc")
+
+
+def test_cc_block_sizes_and_unsplit():
+    x, W = gemm_case(3, 777, 2048, seed=5)
+    for block in (32, 128, 256):
+        for S in (1, 2, 16):
+            check_gemm(x, W, KpCfg.make("cc", split_k=S, block=block, rows=2, k_unroll=2), "cc")
+
+
+# ---- tcgen05 kernel: token counts across the UMMA N range, ragged N and K -----------------
+
+@pytest.mark.parametrize("M", [1, 8, 16, 17, 48, 64, 100, 128, 129, 256])
+@pytest.mark.parametrize("N,K", [(136, 7168), (1000, 1032), (4096, 1024)])
+def test_tc05_shapes(M, N, K):
+    x, W = gemm_case(M, N, K, seed=100 + M)
+    check_gemm(x, W, KpCfg.make("tc05"), "tc05")
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 64, 152, 400])
+def test_tc05_stream_k_splits(ctas):
+    # few CTAs (several whole tiles each) to many (many partial tiles per tile)
+    x, W = gemm_case(24, 520, 4096, seed=7)
+    check_gemm(x, W, KpCfg.make("tc05", ctas=ctas, stages=3), "tc05")
+
+
+def test_tc05_m_above_256_is_sliced():
+    x, W = gemm_case(300, 264, 512, seed=8)
+    check_gemm(x, W, KpCfg.make("tc05"), "tc05")
+
+
+def test_tiny_shapes():
+    x, W = gemm_case(2, 1, 8, seed=9)
+    check_gemm(x, W, KpCfg.make("tc05"), "tc05 N=1 K=8")
+    check_gemm(x, W, KpCfg.make("cc", split_k=1, block=32, rows=1, k_unroll=4), "cc N=1 K=8")
+    check_gemm(x, W, KpCfg.make("smallk", block=64, rows=1), "smallk N=1 K=8")
+
+
+# ---- small-K kernel (the F_B shape) --------------------------------------------------------
+
+@pytest.mark.parametrize("M", [1, 7, 33, 128])
+@pytest.mark.parametrize("N,K,rows", [(1024, 128, 16), (100, 256, 8), (1024, 128, 64)])
+def test_smallk_shapes(M, N, K, rows):
+    x, W = gemm_case(M, N, K, seed=200 + M)
+    check_gemm(x, W, KpCfg.make("smallk", block=256, rows=rows), "smallk")
+
+
+# ---- closed forms through the GPU path -----------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [KpCfg.make("cc", split_k=7, rows=4, k_unroll=2),
+                                 KpCfg.make("tc05"), None])
+def test_all_ones_gives_k_exactly(cfg):
+    M, N, K = 4, 300, 7168
+    x = torch.ones((M, K), dtype=torch.bfloat16, device="cuda")
+    W = torch.ones((N, K), dtype=torch.bfloat16, device="cuda")
+    y = poisoned((M, N))
+    binding.skinny_gemm(x, W, y, cfg=cfg)
+    torch.cuda.synchronize()
+    assert torch.equal(y.float().cpu(), torch.full((M, N), 7168.0))
+
+
+def test_one_hot_selects_a_weight_column():
+    M, N, K = 5, 640, 2048
+    W = gen_w(N, K, seed=3, std=1.0)
+    cols = [0, 17, 1000, 2047, 64]
+    x = torch.zeros((M, K))
+    for m, j in enumerate(cols):
+        x[m, j] = 1.0
+    x = x.to(torch.bfloat16)
+    for cfg in (KpCfg.make("cc", split_k=4, rows=2, k_unroll=2), KpCfg.make("tc05")):
+        y = poisoned((M, N))
+        binding.skinny_gemm(x.cuda(), W.cuda(), y, cfg=cfg)
+        torch.cuda.synchronize()
+        for m, j in enumerate(cols):
+            assert torch.equal(y[m].cpu(), W[:, j])
+
+
+# ---- the full KDA projection at the pages' per-rank shapes --------------------------------
+
+@pytest.fixture(scope="module")
+def plan():
+    p = binding.KdaPlan(K=7168, N_qkvg=4096, N_fab=136, N_fb=1024, max_M=256)
+    yield p
+    p.close()
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_kda_full_size_overlapped(plan, M):
+    x, wp, wfb = kda_inputs(M, layer=0)
+    aux = torch.cuda.Stream()
+    evs = binding.make_events()
+    outs = (poisoned((M, 4096)), poisoned((M, 136)), poisoned((M, 1024)))
+    plan.set_overlap(1)
+    try:
+        plan.run(x.cuda(), wp.cuda(), wfb.cuda(), *outs, aux_stream=aux, events=evs)
+        torch.cuda.synchronize()
+    finally:
+        plan.set_overlap(-1)
+    check_kda(outs, x, wp, wfb, 4096, 136, f"M={M}")
+
+
+@pytest.mark.parametrize("M", [3, 13, 129, 256])
+def test_kda_other_token_counts(plan, M):
+    x, wp, wfb = kda_inputs(M, layer=5, seed=2)
+    outs = (poisoned((M, 4096)), poisoned((M, 136)), poisoned((M, 1024)))
+    plan.run(x.cuda(), wp.cuda(), wfb.cuda(), *outs)
+    torch.cuda.synchronize()
+    check_kda(outs, x, wp, wfb, 4096, 136, f"M={M}")
+
+
+def test_kda_last_layer_of_the_stack(plan):
+    # the benchmark rotates through 48 layers; layer 47 has its own seed
+    x, wp, wfb = kda_inputs(16, layer=47)
+    outs = plan.run(x.cuda(), wp.cuda(), wfb.cuda())
+    torch.cuda.synchronize()
+    check_kda(outs, x, wp, wfb, 4096, 136, "layer 47")
+
+
+def test_kda_small_packed_shapes():
+    # ragged Q/K/V/G width, F_A/beta width 136, non-multiple-of-64 K
+    p = binding.KdaPlan(K=1032, N_qkvg=1000, N_fab=136, N_fb=200, max_M=40)
+    try:
+        for M in (1, 9, 40):
+            x, wp, wfb = kda_inputs(M, layer=1, seed=4, K=1032, Nq=1000, Nfab=136, Nfb=200)
+            outs = (poisoned((M, 1000)), poisoned((M, 136)), poisoned((M, 200)))
+            p.run(x.cuda(), wp.cuda(), wfb.cuda(), *outs, aux_stream=torch.cuda.Stream(),
+                  events=binding.make_events())
+            torch.cuda.synchronize()
+            check_kda(outs, x, wp, wfb, 1000, 136, f"small M={M}")
+    finally:
+        p.close()
+
+
+def test_kda_chain_closed_form():
+    # x = 1, Q/K/V/G rows 2^-10, F_A/beta rows 1 + 2^-7, W_fb = 1, K = 7168:
+    # qkvg = 7, fab = 7224 -> bf16 7232, fb = 128 * 7232 = 925696 (the bf16 of
+    # 925696 is 925696: 0x4962 = 1.765625 * 2^19)
+    M = 3
+    p = binding.KdaPlan(K=7168, N_qkvg=256, N_fab=136, N_fb=64, max_M=M)
+    try:
+        x = torch.ones((M, 7168), dtype=torch.bfloat16, device="cuda")
+        wp = torch.cat([torch.full((256, 7168), 2.0 ** -10), torch.full((136, 7168), 1 + 2.0 ** -7)])
+        wp = wp.to(torch.bfloat16).cuda()
+        wfb = torch.ones((64, 128), dtype=torch.bfloat16, device="cuda")
+        oq, of, ob = p.run(x, wp, wfb)
+        torch.cuda.synchronize()
+        assert torch.equal(oq.float().cpu(), torch.full((M, 256), 7.0))
+        assert torch.equal(of.float().cpu(), torch.full((M, 136), 7232.0))
+        assert torch.equal(ob.float().cpu(), torch.full((M, 64), 925696.0))
+    finally:
+        p.close()
+
+
+# ---- bit identity: sequential == overlapped == graph replay == PDL off ---------------------
+
+def _run(plan, x, wp, wfb, overlap, aux, evs):
+    M = x.shape[0]
+    outs = (poisoned((M, 4096)), poisoned((M, 136)), poisoned((M, 1024)))
+    plan.set_overlap(1 if overlap else 0)
+    plan.run(x, wp, wfb, *outs, aux_stream=aux, events=evs)
+    torch.cuda.synchronize()
+    return [o.clone() for o in outs]
+
+
+@pytest.mark.parametrize("M", [1, 4, 14, 16, 64, 128])
+def test_overlap_graph_pdl_bit_identical(plan, M):
+    x, wp, wfb = kda_inputs(M, layer=2, seed=1)
+    x, wp, wfb = x.cuda(), wp.cuda(), wfb.cuda()
+    aux = torch.cuda.Stream()
+    evs = binding.make_events()
+    try:
+        seq = _run(plan, x, wp, wfb, False, aux, evs)
+        ovl = _run(plan, x, wp, wfb, True, aux, evs)
+        again = _run(plan, x, wp, wfb, True, aux, evs)
+        for a, b, c in zip(seq, ovl, again):
+            assert torch.equal(a, b) and torch.equal(a, c)
+
+        # captured and replayed (overlapped: aux joins the capture via events[0])
+        outs = (poisoned((M, 4096)), poisoned((M, 136)), poisoned((M, 1024)))
+        plan.set_overlap(1)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.run(x, wp, wfb, *outs, aux_stream=aux, events=evs)
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(seq, outs):
+            assert torch.equal(a, b)
+
+        # programmatic dependent launch off for every branch
+        saved = [plan.get_config(b, M) for b in range(3)]
+        try:
+            for b, c in enumerate(saved):
+                c2 = KpCfg.from_buffer_copy(c)
+                c2.flags = 0
+                plan.set_config(b, M, c2)
+            nopdl = _run(plan, x, wp, wfb, True, aux, evs)
+        finally:
+            for b, c in enumerate(saved):
+                plan.set_config(b, M, c)
+        for a, b in zip(seq, nopdl):
+            assert torch.equal(a, b)
+    finally:
+        plan.set_overlap(-1)
+
+
+# ---- boundary errors on a live device -------------------------------------------------------
+
+def test_errors_on_device(plan):
+    x, wp, wfb = kda_inputs(2, layer=0)
+    x, wp, wfb = x.cuda(), wp.cuda(), wfb.cuda()
+    # M above the plan's max_M
+    big = torch.zeros((257, 7168), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.KdaProjError) as e:
+        plan.run(big, wp, wfb)
+    assert e.value.code == binding.KP_ETOOBIG
+    # misaligned pointer (2-byte offset)
+    flat = torch.zeros(2 * 7168 + 8, dtype=torch.bfloat16, device="cuda")
+    xm = flat[1:1 + 2 * 7168].view(2, 7168)
+    with pytest.raises(binding.KdaProjError) as e:
+        binding.skinny_gemm(xm, wp[:64].contiguous())
+    assert e.value.code == binding.KP_EALIGN
+    # the CUDA-core kernel is for M <= 16
+    with pytest.raises(binding.KdaProjError) as e:
+        binding.skinny_gemm(torch.zeros((17, 7168), dtype=torch.bfloat16, device="cuda"),
+                            wp[:64].contiguous(), cfg=KpCfg.make("cc", split_k=4, rows=1, k_unroll=4))
+    assert e.value.code == binding.KP_ECONFIG
+    # M = 0 leaves the outputs untouched
+    empty = torch.zeros((0, 7168), dtype=torch.bfloat16, device="cuda")
+    outs = (poisoned((0, 4096)), poisoned((0, 136)), poisoned((0, 1024)))
+    plan.run(empty, wp, wfb, *outs)
+    # a config needing more scratch than the plan holds is refused
+    small = binding.KdaPlan(K=7168, N_qkvg=4096, N_fab=136, N_fb=1024, max_M=2)
+    try:
+        cfg = KpCfg.make("cc", split_k=56, rows=1, k_unroll=4)
+        with pytest.raises(binding.KdaProjError) as e:
+            small.set_config(binding.BRANCH_QKVG, 2, cfg)
+        assert e.value.code == binding.KP_ETOOBIG
+    finally:
+        small.close()
+
+
+def test_repeat_calls_bit_identical():
+    x, W = gemm_case(6, 4096, 7168, seed=11)
+    x, W = x.cuda(), W.cuda()
+    for cfg in (KpCfg.make("cc", split_k=7, rows=4, k_unroll=2), KpCfg.make("tc05")):
+        a = binding.skinny_gemm(x, W, cfg=cfg)
+        b = binding.skinny_gemm(x, W, cfg=cfg)
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
