@@ -177,7 +177,7 @@ def run_ours(args):
     barrier(dist)
     binding.load()
     hbm_peak, tc_peak, peak_src = load_peaks()
-    m_list = [m for m in M_LIST if m <= args.max_m]
+    m_list = args.m or [m for m in M_LIST if m <= args.max_m]
     L = args.layers
 
     # weights: layer 0 from the canonical CPU stream, the rest drawn on the GPU
@@ -193,7 +193,7 @@ def run_ours(args):
                 torch.empty((M, N_FAB), dtype=torch.bfloat16, device=dev),
                 torch.empty((M, N_FB), dtype=torch.bfloat16, device=dev)) for M in m_list}
 
-    plan = binding.KdaPlan(K, N_QKVG, N_FAB, N_FB, max_M=max(m_list))
+    plan = binding.KdaPlan(K, N_QKVG, N_FAB, N_FB, max_M=max(max(m_list), 128))
     main = torch.cuda.Stream(device=dev)
     aux = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(main):
@@ -305,7 +305,7 @@ def run_ours(args):
     q_bytes = sum(qkvg_bytes(M) for M in keys)
     q_time_us = sum(per_m[str(M)]["qkvg_kernel_us"] for M in keys)
     achieved = q_bytes / (q_time_us * 1e3)  # GB/s
-    cpu = run_cpu_baseline(args) if (rank == 0 and not args.no_cpu) else None
+    cpu = run_cpu_baseline(args, m_list) if (rank == 0 and not args.no_cpu) else None
     plan.close()
     if rank == 0:
         line = {
@@ -428,13 +428,13 @@ def oracle_step(stride: int, nthreads: int, m_list):
     return statistics.fmean(times)
 
 
-def run_cpu_baseline(args):
+def run_cpu_baseline(args, m_list):
     nthreads = os.cpu_count() or 1
     stride = 1
-    t = oracle_step(stride, nthreads, [m for m in M_LIST if m <= args.max_m])
+    t = oracle_step(stride, nthreads, m_list)
     return {"value": round(t * 1e6, 1), "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": f"double-precision oracle, full projection (all output features), one "
-                      f"call per M in {list(M_LIST)} on layer 0, {nthreads} threads over output "
+                      f"call per M in {list(m_list)} on layer 0, {nthreads} threads over output "
                       f"features; mean over M"}
 
 
@@ -444,7 +444,7 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    m_list = [m for m in M_LIST if m <= args.max_m]
+    m_list = args.m or [m for m in M_LIST if m <= args.max_m]
     nthreads = os.cpu_count() or 1
     for _ in range(args.warmup):
         oracle_step(args.cpu_stride * 4, nthreads, m_list[:1])
@@ -479,6 +479,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--max-m", type=int, default=128)
+    ap.add_argument("--m", type=int, nargs="*", default=None,
+                    help="token counts to run (default 1 2 4 ... 128 up to --max-m)")
     ap.add_argument("--cmp-steps", type=int, default=20,
                     help="steps for the sequential/overlapped/kernel-alone comparisons")
     ap.add_argument("--cpu-stride", type=int, default=16,

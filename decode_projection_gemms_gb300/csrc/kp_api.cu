@@ -136,10 +136,7 @@ static kp_cfg builtin_config(int M, int N, int K, int sms) {
         c.split_k = S;
         if (cc_supported(M, K, c)) return c;
     }
-    memset(&c, 0, sizeof c);
-    c.flags = KP_FLAG_PDL;
-    c.kind = KP_KIND_TC05;
-    return c;
+    return tc05_default(M, N, K, sms);
 }
 
 static kp_cfg select_config(int M, int N, int K, int sms, int *overlap) {

@@ -51,8 +51,10 @@ __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
         wrow[r] = a.W + static_cast<int64_t>(n) * a.K + k0;
     }
 
-    uint4 w[R][U];
-    auto load_batch = [&](int c0) {
+    // Two batches of U chunks per row in flight per warp (double buffering):
+    // the next batch is requested before the current one is consumed.
+    uint4 wa[R][U], wb[R][U];
+    auto load_batch = [&](uint4 (&w)[R][U], int c0) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int c = c0 + 32 * u;
@@ -62,31 +64,13 @@ __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
         }
     };
 
-    // Weights never depend on the previous kernel: start streaming them
-    // before waiting for it.
-    load_batch(lane);
-    pdl_wait();
-    pdl_trigger();
-
-    // Stage x[0:M, k0:k0+klen] as fp32.
-    for (int i = threadIdx.x; i < M * nchunk; i += blockDim.x) {
-        const int m = i / nchunk;
-        const int c = i - m * nchunk;
-        const uint4 v = *reinterpret_cast<const uint4 *>(a.x + m * a.ldx + k0 + 8 * c);
-        float4 *d = reinterpret_cast<float4 *>(xs + m * p.Ks + 8 * c);
-        d[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
-        d[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
-    }
-    __syncthreads();
-
     float acc[R][M];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
 
-    for (int c0 = lane; c0 < nchunk; c0 += 32 * U) {
-        if (c0 != lane) load_batch(c0);
+    auto compute = [&](const uint4 (&w)[R][U], int c0) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int c = c0 + 32 * u;
@@ -120,6 +104,32 @@ __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
                 }
             }
         }
+    };
+
+    // Weights never depend on the previous kernel: start streaming them
+    // before waiting for it.
+    load_batch(wa, lane);
+    pdl_wait();
+    pdl_trigger();
+
+    // Stage x[0:M, k0:k0+klen] as fp32.
+    for (int i = threadIdx.x; i < M * nchunk; i += blockDim.x) {
+        const int m = i / nchunk;
+        const int c = i - m * nchunk;
+        const uint4 v = *reinterpret_cast<const uint4 *>(a.x + m * a.ldx + k0 + 8 * c);
+        float4 *d = reinterpret_cast<float4 *>(xs + m * p.Ks + 8 * c);
+        d[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+        d[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+    }
+    __syncthreads();
+
+    for (int c0 = lane; c0 < nchunk; c0 += 64 * U) {
+        const int c1 = c0 + 32 * U;
+        const int c2 = c1 + 32 * U;
+        if (c1 < nchunk) load_batch(wb, c1);
+        compute(wa, c0);
+        if (c2 < nchunk) load_batch(wa, c2);
+        if (c1 < nchunk) compute(wb, c1);
     }
 
     // Butterfly reduction over the 32 lanes: every lane ends with the sums.
@@ -172,8 +182,19 @@ __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
         const int m = i / p.rows_cta;
         const int n = tile_row0 + (i - m * p.rows_cta);
         if (n >= a.N) continue;
+        // partials summed in slice order 0..S-1; loads issued 8 at a time
         float t = 0.f;
-        for (int q = 0; q < p.S; ++q) t += __ldcg(a.ws + (static_cast<int64_t>(q) * M + m) * a.N + n);
+        for (int q0 = 0; q0 < p.S; q0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = (q0 + j < p.S)
+                           ? __ldcg(a.ws + (static_cast<int64_t>(q0 + j) * M + m) * a.N + n)
+                           : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (q0 + j < p.S) t += v[j];
+        }
         a.y[m * a.ldy + n] = __float2bfloat16_rn(t);
     }
     if (threadIdx.x == 0) a.counters[tile] = 0;  // ready for the next launch

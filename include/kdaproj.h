@@ -82,7 +82,7 @@ enum kp_status {
 enum kp_kind {
     KP_KIND_AUTO = 0,  /* look the shape up in the table (or the built-in rule) */
     KP_KIND_CC = 1,    /* CUDA-core split-K weight-streaming GEMV, M <= 16 */
-    KP_KIND_TC05 = 2,  /* TMA-fed tcgen05/TMEM stream-K tile kernel, any M */
+    KP_KIND_TC05 = 2,  /* TMA-fed tcgen05/TMEM cluster split-K tile kernel */
     KP_KIND_SMALLK = 3 /* CUDA-core small-K kernel (K <= 256), the F_B shape */
 };
 
@@ -96,12 +96,18 @@ enum kp_flags {
 /* One kernel configuration. Fields a kind does not use are ignored. */
 typedef struct kp_cfg {
     int32_t kind;     /* enum kp_kind */
-    int32_t split_k;  /* CC: number of K slices S >= 1 (S > 1 uses scratch) */
-    int32_t block;    /* CC, SMALLK: threads per CTA (multiple of 32, <= 1024) */
+    int32_t split_k;  /* CC: number of K slices S >= 1 (S > 1 uses scratch);
+                         TC05: CTAs per thread-block cluster sharing one
+                         128-feature tile, each streaming 1/split_k of K
+                         (1, 2, 4, 8, 16; reduced in distributed shared
+                         memory, no scratch) */
+    int32_t block;    /* CC, SMALLK: threads per CTA (multiple of 32; CC <= 256,
+                         SMALLK <= 256) */
     int32_t rows;     /* CC: output rows per warp (1, 2, 4, 8);
                          SMALLK: output rows per CTA (1..64) */
-    int32_t k_unroll; /* CC: 16-byte W loads in flight per row per lane (1, 2, 4) */
-    int32_t ctas;     /* TC05: persistent CTAs (0 = one per SM) */
+    int32_t k_unroll; /* CC: 16-byte W loads in flight per row per lane (1, 2, 4);
+                         TC05: 64-wide K blocks per pipeline stage (1, 2, 4) */
+    int32_t ctas;     /* reserved, 0 */
     int32_t stages;   /* TC05: shared-memory pipeline stages (0 = as many as fit) */
     int32_t flags;    /* enum kp_flags */
 } kp_cfg;

@@ -87,8 +87,8 @@ def test_table_lookup_rounds_m_up(lib, tmp_path):
         "# M N K kind split_k block rows k_unroll ctas stages flags overlap\n"
         "1 4096 7168 cc 7 256 4 2 0 0 1 1\n"
         "4 4096 7168 cc 5 128 2 4 0 0 1 1  # trailing comment\n"
-        "16 4096 7168 tc05 1 0 0 0 148 6 1 0\n"
-        "64 4096 7168 tc05 1 0 0 0 152 4 0 1\n")
+        "16 4096 7168 tc05 4 0 0 2 0 3 1 0\n"
+        "64 4096 7168 tc05 2 0 0 1 0 4 0 1\n")
     binding.table_load(str(t))
     try:
         assert binding.table_size() == 4
@@ -99,12 +99,12 @@ def test_table_lookup_rounds_m_up(lib, tmp_path):
             assert (c.kind, c.split_k, c.block, c.rows) == (binding.KIND_CC, 5, 128, 2)
         for M in (5, 9, 16):
             c = binding.select_config(M, 4096, 7168, 152)
-            assert (c.kind, c.ctas, c.stages) == (binding.KIND_TC05, 148, 6)
+            assert (c.kind, c.split_k, c.k_unroll, c.stages) == (binding.KIND_TC05, 4, 2, 3)
         c = binding.select_config(33, 4096, 7168, 152)
-        assert (c.kind, c.ctas, c.stages, c.flags) == (binding.KIND_TC05, 152, 4, 0)
+        assert (c.kind, c.split_k, c.k_unroll, c.stages, c.flags) == (binding.KIND_TC05, 2, 1, 4, 0)
         # beyond the largest bucket, or another (N, K): built-in rule
         c = binding.select_config(100, 4096, 7168, 152)
-        assert c.kind == binding.KIND_TC05 and c.ctas == 0
+        assert c.kind == binding.KIND_TC05 and c.split_k == 4 and c.stages == 0
         c = binding.select_config(1, 4096, 1024, 152)
         assert c.kind == binding.KIND_CC
     finally:
@@ -128,9 +128,13 @@ def test_scratch_sizes(lib):
     assert binding.scratch_bytes(4, 4096, 7168, cc, 152) == 7 * 4 * 4096 * 4 + (4096 // 32) * 4
     one = binding.KpCfg.make("cc", split_k=1, block=256, rows=4, k_unroll=2)
     assert binding.scratch_bytes(4, 4096, 7168, one, 152) == 0
-    tc = binding.KpCfg.make("tc05", ctas=152, stages=4)
-    # G x 2 partial tiles of Mpad x 128 fp32 + one counter per 128-row tile
-    assert binding.scratch_bytes(20, 4096, 7168, tc, 152) == 152 * 2 * 32 * 128 * 4 + 32 * 4
+    tc = binding.KpCfg.make("tc05", split_k=4, k_unroll=2, stages=3)
+    # cluster split-K reduces in distributed shared memory: no scratch
+    assert binding.scratch_bytes(20, 4096, 7168, tc, 152) == 0
+    for bad_tc in (binding.KpCfg.make("tc05", split_k=3), binding.KpCfg.make("tc05", split_k=32),
+                   binding.KpCfg.make("tc05", k_unroll=3), binding.KpCfg.make("tc05", stages=99)):
+        with pytest.raises(binding.KdaProjError):
+            binding.scratch_bytes(20, 4096, 7168, bad_tc, 152)
     bad = binding.KpCfg.make("cc", split_k=1, block=256, rows=8, k_unroll=1)
     with pytest.raises(binding.KdaProjError) as e:
         binding.scratch_bytes(16, 4096, 7168, bad, 152)     # 8 x 16 accumulators: not built

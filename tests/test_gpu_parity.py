@@ -48,10 +48,17 @@ def test_config1_cc(R, U, S):
     check_gemm(x, W, KpCfg.make("cc", split_k=S, block=256, rows=R, k_unroll=U), "cc")
 
 
-@pytest.mark.parametrize("ctas,stages", [(0, 0), (37, 2), (152, 4), (5, 3)])
-def test_config1_tc05(ctas, stages):
+@pytest.mark.parametrize("C,nkb,stages", [(1, 1, 0), (2, 4, 2), (4, 2, 3), (16, 4, 0), (8, 1, 5),
+                                           (32, 1, 0)])
+def test_config1_tc05(C, nkb, stages):
     x, W = config1()
-    check_gemm(x, W, KpCfg.make("tc05", ctas=ctas, stages=stages), "tc05")
+    cfg = KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=stages)
+    if C == 32:  # clusters hold at most 16 CTAs
+        with pytest.raises(binding.KdaProjError) as e:
+            binding.skinny_gemm(x.cuda(), W.cuda(), cfg=cfg)
+        assert e.value.code == binding.KP_ECONFIG
+        return
+    check_gemm(x, W, cfg, "tc05")
 
 
 # ---- CUDA-core kernel: every M bucket, ragged N, several K -------------------------------
@@ -78,28 +85,46 @@ def test_cc_block_sizes_and_unsplit():
 
 # ---- tcgen05 kernel: token counts across the UMMA N range, ragged N and K -----------------
 
+TC05_VARIANTS = [(1, 2), (4, 1), (16, 4), (8, 2)]
+
+
+def _tc05_ok(M, N, K, cfg):
+    try:
+        binding.scratch_bytes(M, N, K, cfg, 152)
+        return True
+    except binding.KdaProjError:
+        return False
+
+
 @pytest.mark.parametrize("M", [1, 8, 16, 17, 48, 64, 100, 128, 129, 256])
 @pytest.mark.parametrize("N,K", [(136, 7168), (1000, 1032), (4096, 1024)])
 def test_tc05_shapes(M, N, K):
     x, W = gemm_case(M, N, K, seed=100 + M)
-    check_gemm(x, W, KpCfg.make("tc05"), "tc05")
+    ran = 0
+    for C, nkb in TC05_VARIANTS:
+        cfg = KpCfg.make("tc05", split_k=C, k_unroll=nkb)
+        if _tc05_ok(M, N, K, cfg):
+            check_gemm(x, W, cfg, "tc05")
+            ran += 1
+    assert ran >= 2
 
 
-@pytest.mark.parametrize("ctas", [1, 3, 64, 152, 400])
-def test_tc05_stream_k_splits(ctas):
-    # few CTAs (several whole tiles each) to many (many partial tiles per tile)
-    x, W = gemm_case(24, 520, 4096, seed=7)
-    check_gemm(x, W, KpCfg.make("tc05", ctas=ctas, stages=3), "tc05")
+@pytest.mark.parametrize("C", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("nkb", [1, 2, 4])
+def test_tc05_cluster_splits(C, nkb):
+    # K = 4096 -> 64 K blocks: uneven stage tails for nkb = 4 when C = 16 (4 blocks each)
+    x, W = gemm_case(24, 520, 4096 + 64 * 3, seed=7)
+    check_gemm(x, W, KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=2), "tc05")
 
 
 def test_tc05_m_above_256_is_sliced():
     x, W = gemm_case(300, 264, 512, seed=8)
-    check_gemm(x, W, KpCfg.make("tc05"), "tc05")
+    check_gemm(x, W, KpCfg.make("tc05", split_k=4, k_unroll=1), "tc05")
 
 
 def test_tiny_shapes():
     x, W = gemm_case(2, 1, 8, seed=9)
-    check_gemm(x, W, KpCfg.make("tc05"), "tc05 N=1 K=8")
+    check_gemm(x, W, KpCfg.make("tc05", split_k=1, k_unroll=1), "tc05 N=1 K=8")
     check_gemm(x, W, KpCfg.make("cc", split_k=1, block=32, rows=1, k_unroll=4), "cc N=1 K=8")
     check_gemm(x, W, KpCfg.make("smallk", block=64, rows=1), "smallk N=1 K=8")
 
@@ -116,7 +141,7 @@ def test_smallk_shapes(M, N, K, rows):
 # ---- closed forms through the GPU path -----------------------------------------------------
 
 @pytest.mark.parametrize("cfg", [KpCfg.make("cc", split_k=7, rows=4, k_unroll=2),
-                                 KpCfg.make("tc05"), None])
+                                 KpCfg.make("tc05", split_k=4, k_unroll=4), None])
 def test_all_ones_gives_k_exactly(cfg):
     M, N, K = 4, 300, 7168
     x = torch.ones((M, K), dtype=torch.bfloat16, device="cuda")
@@ -135,7 +160,8 @@ def test_one_hot_selects_a_weight_column():
     for m, j in enumerate(cols):
         x[m, j] = 1.0
     x = x.to(torch.bfloat16)
-    for cfg in (KpCfg.make("cc", split_k=4, rows=2, k_unroll=2), KpCfg.make("tc05")):
+    for cfg in (KpCfg.make("cc", split_k=4, rows=2, k_unroll=2),
+                KpCfg.make("tc05", split_k=8, k_unroll=2)):
         y = poisoned((M, N))
         binding.skinny_gemm(x.cuda(), W.cuda(), y, cfg=cfg)
         torch.cuda.synchronize()
@@ -313,7 +339,8 @@ def test_errors_on_device(plan):
 def test_repeat_calls_bit_identical():
     x, W = gemm_case(6, 4096, 7168, seed=11)
     x, W = x.cuda(), W.cuda()
-    for cfg in (KpCfg.make("cc", split_k=7, rows=4, k_unroll=2), KpCfg.make("tc05")):
+    for cfg in (KpCfg.make("cc", split_k=7, rows=4, k_unroll=2),
+                KpCfg.make("tc05", split_k=16, k_unroll=4)):
         a = binding.skinny_gemm(x, W, cfg=cfg)
         b = binding.skinny_gemm(x, W, cfg=cfg)
         torch.cuda.synchronize()
