@@ -8,7 +8,7 @@ back-to-back calls, each on a different layer of a weight stack at least
 median over `trials` of (elapsed / calls).
 
 The table format is one line per measured (M, N, K):
-    M N K kind split_k block rows k_unroll ctas stages flags overlap
+    M N K kind split_k block rows k_unroll producers stages flags overlap
 Usage (on a GB300):
     python -m decode_projection_gemms_gb300.autotune --shapes kda --out tune/gb300_table.txt
 """
@@ -62,8 +62,10 @@ def tc05_candidates(M: int, N: int, K: int, sms: int):
         if T * C > 2 * sms:
             continue
         for nkb in (1, 2, 4):
-            for stages in (0, 2, 3, 4, 6):
-                out.append(KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=stages))
+            for P in sorted({1, min(nkb, 2), nkb}):
+                for stages in (0, 2, 3, 4):
+                    out.append(KpCfg.make("tc05", split_k=C, k_unroll=nkb, producers=P,
+                                          stages=stages))
     return out
 
 
@@ -153,7 +155,7 @@ def sweep_shape(M, N, K, sms, device, kinds, verbose=False):
 
 def table_line(M, N, K, cfg, overlap=1, us=None):
     kind = binding.KIND_NAMES[cfg.kind]
-    s = (f"{M} {N} {K} {kind} {cfg.split_k} {cfg.block} {cfg.rows} {cfg.k_unroll} {cfg.ctas} "
+    s = (f"{M} {N} {K} {kind} {cfg.split_k} {cfg.block} {cfg.rows} {cfg.k_unroll} {cfg.producers} "
          f"{cfg.stages} {cfg.flags} {overlap}")
     return s + (f"  # {us:.3f} us" if us is not None else "")
 
@@ -202,7 +204,7 @@ def main(argv=None):
         with open(args.out, "w") as f:
             f.write("# kdaproj autotune table v1 (measured on "
                     f"{torch.cuda.get_device_name(dev)}, {sms} SMs)\n")
-            f.write("# Each line: M N K kind split_k block rows k_unroll ctas stages flags overlap\n")
+            f.write("# Each line: M N K kind split_k block rows k_unroll producers stages flags overlap\n")
             f.write("# A call with (M, N, K) takes the entry with the same (N, K) and the smallest\n")
             f.write("# M >= its own; shapes without an entry use the library's built-in rule.\n")
             for l in lines:

@@ -46,7 +46,7 @@ class KdaProjError(RuntimeError):
 
 class KpCfg(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("split_k", ctypes.c_int32), ("block", ctypes.c_int32),
-                ("rows", ctypes.c_int32), ("k_unroll", ctypes.c_int32), ("ctas", ctypes.c_int32),
+                ("rows", ctypes.c_int32), ("k_unroll", ctypes.c_int32), ("producers", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
@@ -55,10 +55,11 @@ class KpCfg(ctypes.Structure):
         return d
 
     @classmethod
-    def make(cls, kind, split_k=1, block=256, rows=4, k_unroll=2, ctas=0, stages=0, flags=FLAG_PDL):
+    def make(cls, kind, split_k=1, block=256, rows=4, k_unroll=2, producers=1, stages=0,
+             flags=FLAG_PDL):
         if isinstance(kind, str):
             kind = {v: k for k, v in KIND_NAMES.items()}[kind]
-        return cls(int(kind), int(split_k), int(block), int(rows), int(k_unroll), int(ctas),
+        return cls(int(kind), int(split_k), int(block), int(rows), int(k_unroll), int(producers),
                    int(stages), int(flags))
 
 

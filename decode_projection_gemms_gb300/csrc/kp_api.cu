@@ -192,9 +192,9 @@ static int check_cfg(int M, int N, int K, const kp_cfg &c) {
         return set_error(KP_ECONFIG, "CUDA-core kernel supports M <= 16 (got M=%d)", M);
     if (!cfg_supported(M, N, K, c))
         return set_error(KP_ECONFIG,
-                         "config kind=%d split_k=%d block=%d rows=%d k_unroll=%d ctas=%d stages=%d "
+                         "config kind=%d split_k=%d block=%d rows=%d k_unroll=%d producers=%d stages=%d "
                          "is not valid for M=%d N=%d K=%d",
-                         c.kind, c.split_k, c.block, c.rows, c.k_unroll, c.ctas, c.stages, M, N, K);
+                         c.kind, c.split_k, c.block, c.rows, c.k_unroll, c.producers, c.stages, M, N, K);
     return KP_OK;
 }
 
@@ -263,7 +263,7 @@ int kp_table_load(const char *path) {
         TableEntry e;
         memset(&e, 0, sizeof e);
         int n = sscanf(line, "%d %d %d %31s %d %d %d %d %d %d %d %d", &e.M, &e.N, &e.K, kind,
-                       &e.cfg.split_k, &e.cfg.block, &e.cfg.rows, &e.cfg.k_unroll, &e.cfg.ctas,
+                       &e.cfg.split_k, &e.cfg.block, &e.cfg.rows, &e.cfg.k_unroll, &e.cfg.producers,
                        &e.cfg.stages, &e.cfg.flags, &e.overlap);
         if (n <= 0) continue;  // blank or comment
         if (n != 12 || (e.cfg.kind = parse_kind(kind)) < 0 || e.M < 1 || e.N < 1 || e.K < 8) {

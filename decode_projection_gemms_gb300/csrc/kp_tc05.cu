@@ -22,9 +22,13 @@
 //    small enough for two CTAs per SM, whose producers stream concurrently;
 //  * cta_group::1, no multicast.
 //
-// Warp roles (192 threads): warp 0 = TMA producer (one lane), warp 1 = TMEM
-// allocator + MMA issuer (one lane), warps 2..5 = epilogue (TMEM lane quarter
-// = warp % 4). All 192 threads take part in the cluster reduction.
+// Warp roles (192 threads): warp 1 = TMEM allocator + MMA issuer (one lane),
+// warps 2..5 = epilogue (TMEM lane quarter = warp % 4). TMA copies are issued
+// by lane 0 of P "producer" warps (warp 0, then warps 2, 3, 4, 5): producer
+// p issues the W boxes of K blocks j with j % P == p of every stage, producer
+// 0 also the x box; each arrives once per stage on the stage's barrier. The
+// epilogue warps produce during the main loop and drain the accumulator after
+// it. All 192 threads take part in the cluster reduction.
 //
 // Shared memory per stage: W [nkb][128 rows][128 B] then x [nkb][Mpad rows]
 // [128 B], written by TMA with the 128-byte swizzle, i.e. the K-major
@@ -59,6 +63,7 @@ struct Tc05Params {
     int C;             // CTAs per cluster = K splits per tile
     int nkb;           // K blocks per stage
     int x3d;           // 1: x of a full stage is one 3-D box (K % 64 == 0)
+    int producers;     // warps issuing TMA copies (1..5)
     int stages;
     uint32_t idesc;
     uint32_t tmem_cols;
@@ -107,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(full + s), 1);
+            mbar_init(smem_u32(full + s), static_cast<uint32_t>(p.producers));
             mbar_init(smem_u32(empty + s), 1);
         }
         mbar_init(smem_u32(accf), 1);
@@ -127,57 +132,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
     pdl_trigger();
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer ----------------
-            const uint64_t pol_w = policy_evict_first();
-            const uint64_t pol_x = policy_evict_last();
-            const uint32_t xblk = static_cast<uint32_t>(p.Mpad) * kBlockK * 2;
-            const int row0 = tile * kTileN;
-            // A full stage's x is one 3-D box; a short last stage uses one
-            // 2-D box per K block (so nothing past this CTA's range is read).
-            auto x_full = [&](int kbs) { return p.x3d && kbs == p.nkb; };
-            auto issue_w = [&](int s, int stage) {
-                const int k0 = kb0 + s * p.nkb;
-                const int kbs = min(p.nkb, kb1 - k0);
-                const uint32_t st = base + stage * p.stage_bytes;
-                const uint32_t bar = smem_u32(full + stage);
-                mbar_expect_tx(bar, static_cast<uint32_t>(kbs) * (kWBlockBytes + xblk));
+    // producer index of this warp's lane 0 (-1: not a producer)
+    const int pidx = (warp == 0) ? 0 : (warp >= 2 && warp - 1 < p.producers) ? warp - 1 : -1;
+    if (pidx >= 0 && lane == 0) {
+        // ---------------- TMA producers ----------------
+        const int P = p.producers;
+        const uint64_t pol_w = policy_evict_first();
+        const uint64_t pol_x = policy_evict_last();
+        const uint32_t xblk = static_cast<uint32_t>(p.Mpad) * kBlockK * 2;
+        const int row0 = tile * kTileN;
+        // A full stage's x is one 3-D box; a short last stage uses one 2-D box
+        // per K block (so nothing past this CTA's range is read).
+        auto x_full = [&](int kbs) { return p.x3d && kbs == p.nkb; };
+        auto issue_w = [&](int s, int stage) {
+            const int k0 = kb0 + s * p.nkb;
+            const int kbs = min(p.nkb, kb1 - k0);
+            const uint32_t st = base + stage * p.stage_bytes;
+            const uint32_t bar = smem_u32(full + stage);
+            int mine = 0;
+            for (int j = pidx; j < kbs; j += P) ++mine;
+            uint32_t bytes = static_cast<uint32_t>(mine) * kWBlockBytes;
+            if (pidx == 0) bytes += static_cast<uint32_t>(kbs) * xblk;
+            mbar_expect_tx(bar, bytes);   // every producer arrives once per stage
+            for (int j = pidx; j < kbs; j += P)
+                tma_load_2d(st + j * kWBlockBytes, &tmw, bar, (k0 + j) * kBlockK, row0, pol_w);
+        };
+        auto issue_x = [&](int s, int stage) {
+            const int k0 = kb0 + s * p.nkb;
+            const int kbs = min(p.nkb, kb1 - k0);
+            const uint32_t st = base + stage * p.stage_bytes + p.w_stage_bytes;
+            const uint32_t bar = smem_u32(full + stage);
+            if (x_full(kbs)) {
+                tma_load_3d(st, &tmx3, bar, 0, 0, k0, pol_x);
+            } else {
                 for (int j = 0; j < kbs; ++j)
-                    tma_load_2d(st + j * kWBlockBytes, &tmw, bar, (k0 + j) * kBlockK, row0, pol_w);
-            };
-            auto issue_x = [&](int s, int stage) {
-                const int k0 = kb0 + s * p.nkb;
-                const int kbs = min(p.nkb, kb1 - k0);
-                const uint32_t st = base + stage * p.stage_bytes + p.w_stage_bytes;
-                const uint32_t bar = smem_u32(full + stage);
-                if (x_full(kbs)) {
-                    tma_load_3d(st, &tmx3, bar, 0, 0, k0, pol_x);
-                } else {
-                    for (int j = 0; j < kbs; ++j)
-                        tma_load_2d(st + j * xblk, &tmx, bar, (k0 + j) * kBlockK, 0, pol_x);
-                }
-            };
-            const int pre = n_st < S ? n_st : S;
-            // Weights never depend on the previous kernel: the first stages'
-            // W tiles go out before waiting for it; x follows after.
-            for (int s = 0; s < pre; ++s) issue_w(s, s);
+                    tma_load_2d(st + j * xblk, &tmx, bar, (k0 + j) * kBlockK, 0, pol_x);
+            }
+        };
+        const int pre = n_st < S ? n_st : S;
+        // Weights never depend on the previous kernel: the first stages' W
+        // tiles go out before waiting for it; x (producer 0) follows after.
+        for (int s = 0; s < pre; ++s) issue_w(s, s);
+        if (pidx == 0) {
             pdl_wait();
             for (int s = 0; s < pre; ++s) issue_x(s, s);
-            for (int s = pre; s < n_st; ++s) {
-                const int stage = s % S;
-                mbar_wait_bounded(smem_u32(empty + stage), static_cast<uint32_t>(((s / S) - 1) & 1),
-                                  abort_flag, p.err, DEV_TIMEOUT_EMPTY);
-                issue_w(s, stage);
-                issue_x(s, stage);
-            }
-            if (*abort_flag) {
-                // Something gave up: let our own copies land before exiting.
-                const int first = n_st > S ? n_st - S : 0;
-                for (int s = first; s < n_st; ++s)
-                    drain_wait(smem_u32(full + (s % S)), static_cast<uint32_t>((s / S) & 1));
-            }
         }
+        for (int s = pre; s < n_st; ++s) {
+            const int stage = s % S;
+            mbar_wait_bounded(smem_u32(empty + stage), static_cast<uint32_t>(((s / S) - 1) & 1),
+                              abort_flag, p.err, DEV_TIMEOUT_EMPTY);
+            issue_w(s, stage);
+            if (pidx == 0) issue_x(s, stage);
+        }
+        if (*abort_flag) {
+            // Something gave up: let our own copies land before exiting.
+            const int first = n_st > S ? n_st - S : 0;
+            for (int s = first; s < n_st; ++s)
+                drain_wait(smem_u32(full + (s % S)), static_cast<uint32_t>((s / S) & 1));
+        }
+    }
+    if (warp == 0) {
+        // lanes 1..31 of warp 0 have nothing to do until the end
     } else if (warp == 1) {
         if (lane == 0) {
             // ---------------- MMA issuer ----------------
@@ -207,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;          // TMEM lane quarter this warp may read
         const int row = q * 32 + lane;   // feature row within the tile
         const int n = tile * kTileN + row;
+        __syncwarp();   // lane 0 may have been producing
         pdl_wait();
         mbar_wait_bounded(smem_u32(accf), 0, abort_flag, p.err, DEV_TIMEOUT_ACC_FULL);
         tc_fence_after();
@@ -363,6 +379,7 @@ int max_stages(int Mpad, int nkb) {
 }
 
 int cluster_of(const kp_cfg &c) { return c.split_k < 1 ? 1 : c.split_k; }
+int producers_of(const kp_cfg &c) { return c.producers < 1 ? 1 : c.producers; }
 int nkb_of(const kp_cfg &c) { return c.k_unroll < 1 ? 1 : c.k_unroll; }
 
 }  // namespace
@@ -382,6 +399,7 @@ kp_cfg tc05_default(int M, int N, int K, int num_sms) {
     while (nkb > 1 && max_stages(Mpad, nkb) < 3) nkb /= 2;
     c.split_k = C;
     c.k_unroll = nkb;
+    c.producers = nkb;
     c.stages = 0;
     return c;
 }
@@ -394,6 +412,7 @@ bool tc05_supported(int M, int N, int K, const kp_cfg &c) {
     if (C > KB) return false;
     const int nkb = nkb_of(c);
     if (nkb != 1 && nkb != 2 && nkb != 4) return false;
+    if (c.producers < 0 || c.producers > 5) return false;
     const int Mpad = mpad_of(M);
     const int ms = max_stages(Mpad, nkb);
     const int st = c.stages ? c.stages : ms;
@@ -422,6 +441,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.KB = (a.K + kBlockK - 1) / kBlockK;
     p.C = cluster_of(c);
     p.nkb = nkb;
+    p.producers = producers_of(c);
     p.stages = stages;
     // kind::f16 instruction descriptor: D fp32 (bit 4), A and B bf16 (bits
     // 7, 10), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.

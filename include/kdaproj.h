@@ -107,7 +107,7 @@ typedef struct kp_cfg {
                          SMALLK: output rows per CTA (1..64) */
     int32_t k_unroll; /* CC: 16-byte W loads in flight per row per lane (1, 2, 4);
                          TC05: 64-wide K blocks per pipeline stage (1, 2, 4) */
-    int32_t ctas;     /* reserved, 0 */
+    int32_t producers;/* TC05: warps issuing TMA copies per CTA (1..5; 0 = 1) */
     int32_t stages;   /* TC05: shared-memory pipeline stages (0 = as many as fit) */
     int32_t flags;    /* enum kp_flags */
 } kp_cfg;

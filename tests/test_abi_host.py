@@ -84,10 +84,10 @@ def test_builtin_rule(lib):
 def test_table_lookup_rounds_m_up(lib, tmp_path):
     t = tmp_path / "t.txt"
     t.write_text(
-        "# M N K kind split_k block rows k_unroll ctas stages flags overlap\n"
+        "# M N K kind split_k block rows k_unroll producers stages flags overlap\n"
         "1 4096 7168 cc 7 256 4 2 0 0 1 1\n"
         "4 4096 7168 cc 5 128 2 4 0 0 1 1  # trailing comment\n"
-        "16 4096 7168 tc05 4 0 0 2 0 3 1 0\n"
+        "16 4096 7168 tc05 4 0 0 2 2 3 1 0\n"
         "64 4096 7168 tc05 2 0 0 1 0 4 0 1\n")
     binding.table_load(str(t))
     try:
@@ -99,7 +99,7 @@ def test_table_lookup_rounds_m_up(lib, tmp_path):
             assert (c.kind, c.split_k, c.block, c.rows) == (binding.KIND_CC, 5, 128, 2)
         for M in (5, 9, 16):
             c = binding.select_config(M, 4096, 7168, 152)
-            assert (c.kind, c.split_k, c.k_unroll, c.stages) == (binding.KIND_TC05, 4, 2, 3)
+            assert (c.kind, c.split_k, c.k_unroll, c.producers, c.stages) == (binding.KIND_TC05, 4, 2, 2, 3)
         c = binding.select_config(33, 4096, 7168, 152)
         assert (c.kind, c.split_k, c.k_unroll, c.stages, c.flags) == (binding.KIND_TC05, 2, 1, 4, 0)
         # beyond the largest bucket, or another (N, K): built-in rule
@@ -132,7 +132,8 @@ def test_scratch_sizes(lib):
     # cluster split-K reduces in distributed shared memory: no scratch
     assert binding.scratch_bytes(20, 4096, 7168, tc, 152) == 0
     for bad_tc in (binding.KpCfg.make("tc05", split_k=3), binding.KpCfg.make("tc05", split_k=32),
-                   binding.KpCfg.make("tc05", k_unroll=3), binding.KpCfg.make("tc05", stages=99)):
+                   binding.KpCfg.make("tc05", k_unroll=3), binding.KpCfg.make("tc05", stages=99),
+                   binding.KpCfg.make("tc05", producers=6)):
         with pytest.raises(binding.KdaProjError):
             binding.scratch_bytes(20, 4096, 7168, bad_tc, 152)
     bad = binding.KpCfg.make("cc", split_k=1, block=256, rows=8, k_unroll=1)

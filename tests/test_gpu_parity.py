@@ -85,7 +85,7 @@ def test_cc_block_sizes_and_unsplit():
 
 # ---- tcgen05 kernel: token counts across the UMMA N range, ragged N and K -----------------
 
-TC05_VARIANTS = [(1, 2), (4, 1), (16, 4), (8, 2)]
+TC05_VARIANTS = [(1, 2, 1), (4, 1, 1), (16, 4, 4), (8, 2, 2), (4, 4, 3)]
 
 
 def _tc05_ok(M, N, K, cfg):
@@ -101,8 +101,8 @@ def _tc05_ok(M, N, K, cfg):
 def test_tc05_shapes(M, N, K):
     x, W = gemm_case(M, N, K, seed=100 + M)
     ran = 0
-    for C, nkb in TC05_VARIANTS:
-        cfg = KpCfg.make("tc05", split_k=C, k_unroll=nkb)
+    for C, nkb, P in TC05_VARIANTS:
+        cfg = KpCfg.make("tc05", split_k=C, k_unroll=nkb, producers=P)
         if _tc05_ok(M, N, K, cfg):
             check_gemm(x, W, cfg, "tc05")
             ran += 1
@@ -112,9 +112,11 @@ def test_tc05_shapes(M, N, K):
 @pytest.mark.parametrize("C", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("nkb", [1, 2, 4])
 def test_tc05_cluster_splits(C, nkb):
-    # K = 4096 -> 64 K blocks: uneven stage tails for nkb = 4 when C = 16 (4 blocks each)
+    # K = 4288 -> 67 K blocks: uneven ranges per cluster rank and short last stages
     x, W = gemm_case(24, 520, 4096 + 64 * 3, seed=7)
-    check_gemm(x, W, KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=2), "tc05")
+    for P in sorted({1, 2, nkb, 5}):
+        check_gemm(x, W, KpCfg.make("tc05", split_k=C, k_unroll=nkb, producers=P, stages=2),
+                   f"tc05 P={P}")
 
 
 def test_tc05_m_above_256_is_sliced():
