@@ -34,7 +34,7 @@ EXPORTS = (
     "skinny_gemm", "kp_select_config", "kp_table_load", "kp_table_clear", "kp_table_size",
     "kda_proj_plan", "kda_proj_set_overlap", "kda_proj_get_config", "kda_proj_set_config",
     "kda_proj_overlap_at", "kda_proj_run", "kda_proj_destroy", "kp_last_error", "kp_version",
-    "kp_device_error", "kp_scratch_bytes",
+    "kp_device_error", "kp_scratch_bytes", "skinny_gemm_noalloc",
 )
 
 
@@ -95,6 +95,7 @@ def load(path: str | None = None):
             "kp_version": [],
             "kp_device_error": [ctypes.POINTER(ci)],
             "kp_scratch_bytes": [ci, ci, ci, cfgp, ci, ctypes.POINTER(ctypes.c_size_t)],
+            "skinny_gemm_noalloc": [vp, vp, vp, ci, ci, ci, cfgp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -181,6 +182,25 @@ def skinny_gemm(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None,
     _check(load().skinny_gemm(x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K,
                               ctypes.byref(cfg) if cfg is not None else None,
                               _stream_handle(stream)))
+    return y
+
+
+def skinny_gemm_noalloc(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor,
+                        cfg: KpCfg | None = None, stream=None) -> torch.Tensor:
+    """``y = bf16(x @ W.T)`` without any allocation by the library: the
+    CUDA-core split-K kernel keeps its partial sums in a fixed device array
+    (for callers that cannot allocate, e.g. during graph capture). ``y`` must
+    be given; M <= 16. Concurrent calls on one device race."""
+    _bf16_2d(x, "x")
+    _bf16_2d(W, "W")
+    _bf16_2d(y, "y")
+    M, K = x.shape
+    N = W.shape[0]
+    if W.shape[1] != K or tuple(y.shape) != (M, N):
+        raise ValueError("shape mismatch")
+    _check(load().skinny_gemm_noalloc(x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K,
+                                      ctypes.byref(cfg) if cfg is not None else None,
+                                      _stream_handle(stream)))
     return y
 
 

@@ -25,6 +25,7 @@ SOURCES = [
     "kp_cc_inst_hi.cu",
     "kp_tc05.cu",
     "kp_smallk.cu",
+    "kp_noalloc.cu",
 ]
 HEADERS = ["kp_internal.cuh", "kp_cc_kernel.cuh"]
 

@@ -147,6 +147,39 @@ KP_API int kp_table_clear(void);
 KP_API int kp_table_size(void);
 
 /* ---------------------------------------------------------------------------
+ * skinny_gemm_noalloc: the same product as skinny_gemm, computed by the
+ * CUDA-core split-K kernel, with its scratch in a fixed device array that the
+ * library itself carries, so the call never allocates. (The pages have no
+ * counterpart: this entry point exists for callers of this library.)
+ *
+ * Meant for callers that cannot call cudaMalloc: code running inside CUDA
+ * graph capture, processes whose device memory is managed by a pooling
+ * allocator, and latency-critical paths that cannot take cudaMalloc's device
+ * synchronisation. The caller still passes x, W and y (same layout as
+ * skinny_gemm); the call calls no cudaMalloc, cudaFree or allocating library
+ * routine.
+ *   - Limits: M <= 16 (CUDA-core kernel); the split-K partial sums
+ *     (split_k * M * N floats) must fit in KP_NOALLOC_SCRATCH_FLOATS and the
+ *     row tiles in KP_NOALLOC_TICKETS; larger needs return KP_ETOOBIG. With
+ *     cfg NULL (or kind AUTO) a CUDA-core configuration that fits is chosen;
+ *     an explicit cfg must be kind KP_KIND_CC.
+ *   - Memory: every GPU that loads the library holds the array
+ *     (2 MiB + 32 KiB) until the process exits.
+ *   - First call per device: looks up the array's device address and zeroes
+ *     its tickets (synchronises that device); make it before any stream
+ *     capture. Later calls only launch the kernel.
+ *   - Sharing: all calls on a device use the same array and it keeps the last
+ *     call's partial sums; calls that overlap on the GPU (different streams,
+ *     or concurrent graph branches) race and give wrong results. Serialise
+ *     them.
+ * Returns KP_OK, KP_EINVAL, KP_EALIGN, KP_ESHAPE, KP_ECONFIG, KP_ETOOBIG,
+ * KP_ENODEV, KP_ECUDA. */
+#define KP_NOALLOC_SCRATCH_FLOATS (1 << 19)
+#define KP_NOALLOC_TICKETS 8192
+KP_API int skinny_gemm_noalloc(const void *x, const void *W, void *y, int M, int N, int K,
+                               const kp_cfg *cfg, kp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * kda_proj_plan: prepare the projection for hidden size K, N_qkvg Q/K/V/G
  * rows, N_fab F_A/beta rows (the first 128 are F_A) and N_fb F_B rows, for
  * token counts 1..max_M. Picks a configuration per (branch, M) from the table,
