@@ -153,6 +153,111 @@ def sweep_shape(M, N, K, sms, device, kinds, verbose=False):
     return results
 
 
+class PlanBench:
+    """Full KDA projection timing: a weight stack of packed [N_qkvg+N_fab, K]
+    + W_fb [N_fb, 128] layers (at least 4x L2), graph of `layers` calls."""
+
+    def __init__(self, max_M, device, K=7168, Nq=4096, Nfab=136, Nfb=1024, seed=0):
+        self.K, self.Nq, self.Nfab, self.Nfb = K, Nq, Nfab, Nfb
+        per = ((Nq + Nfab) * K + Nfb * 128) * 2
+        self.layers = max(4, math.ceil(4 * L2_BYTES / per))
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.Wp = (torch.randn((self.layers, Nq + Nfab, K), generator=g, device=device) * 0.02).to(torch.bfloat16)
+        self.Wfb = (torch.randn((self.layers, Nfb, 128), generator=g, device=device) * 0.02).to(torch.bfloat16)
+        self.device = device
+        self.plan = binding.KdaPlan(K, Nq, Nfab, Nfb, max_M=max_M)
+        self.stream = torch.cuda.Stream(device=device)
+        self.aux = torch.cuda.Stream(device=device)
+        with torch.cuda.stream(self.stream):
+            self.evs = binding.make_events()
+
+    def time_call(self, M, mode, reps=10, trials=3):
+        """us per projection call at M tokens with the plan's current configs;
+        mode 1 = overlapped, 0 = sequential."""
+        x = torch.randn((M, self.K), device=self.device).to(torch.bfloat16)
+        outs = self.plan.outputs(M, self.device)
+        self.plan.set_overlap(mode)
+        try:
+            with torch.cuda.stream(self.stream):
+                self.plan.run(x, self.Wp[0], self.Wfb[0], *outs, aux_stream=self.aux, events=self.evs)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                for l in range(self.layers):
+                    self.plan.run(x, self.Wp[l], self.Wfb[l], *outs, aux_stream=self.aux,
+                                  events=self.evs)
+            res = []
+            with torch.cuda.stream(self.stream):
+                g.replay()
+                for _ in range(trials):
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(self.stream)
+                    for _ in range(reps):
+                        g.replay()
+                    b.record(self.stream)
+                    b.synchronize()
+                    res.append(a.elapsed_time(b) * 1e3 / (reps * self.layers))
+            del g
+            return statistics.median(res)
+        finally:
+            self.plan.set_overlap(-1)
+
+
+def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
+    """Joint choice per M of the Q/K/V/G, F_A/beta and F_B configurations that
+    minimise the overlapped projection (the aux branch must co-run with the
+    main one), and the per-M overlap flag (overlapped vs sequential with the
+    same configurations)."""
+    pb = PlanBench(max(ms), device)
+    lines, dump = [], []
+    for M in ms:
+        q_res = sweep_shape(M, pb.Nq, pb.K, sms, device, ("cc", "tc05"))[:top_q]
+        b_res = sweep_shape(M, pb.Nfb, 128, sms, device, ("cc", "tc05", "smallk"))[:top_b]
+        f_cands = []
+        for C in (1, 2, 4, 8, 16):
+            for nkb in (2, 4):
+                for stages in (2, 3):
+                    f_cands.append(KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=stages))
+        if M <= 16:
+            f_cands += [c for c in cc_candidates(M, pb.Nfab, pb.K, sms) if c.split_k <= 8]
+        best = None
+        for (_, cq), (_, cb), cf in itertools.product(q_res, b_res, f_cands):
+            try:
+                binding.scratch_bytes(M, pb.Nfab, pb.K, cf, sms)
+                pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
+                pb.plan.set_config(binding.BRANCH_FAB, M, cf)
+                pb.plan.set_config(binding.BRANCH_FB, M, cb)
+                us = pb.time_call(M, 1)
+            except binding.KdaProjError as e:
+                if verbose:
+                    print(f"  skip {cf.as_dict()}: {e}", file=sys.stderr)
+                continue
+            if verbose:
+                print(f"  M={M} overlapped {us:8.3f} us  q={cq.as_dict()} f={cf.as_dict()} b={cb.as_dict()}",
+                      file=sys.stderr)
+            if best is None or us < best[0]:
+                best = (us, cq, cf, cb)
+        us_ovl, cq, cf, cb = best
+        pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
+        pb.plan.set_config(binding.BRANCH_FAB, M, cf)
+        pb.plan.set_config(binding.BRANCH_FB, M, cb)
+        us_ovl = pb.time_call(M, 1)
+        us_seq = pb.time_call(M, 0)
+        ov = 1 if us_ovl < us_seq else 0
+        lines += [table_line(M, pb.Nq, pb.K, cq, ov, us_ovl),
+                  table_line(M, pb.Nfab, pb.K, cf, ov),
+                  table_line(M, pb.Nfb, 128, cb, ov)]
+        dump.append({"M": M, "overlapped_us": us_ovl, "sequential_us": us_seq,
+                     "qkvg": cq.as_dict(), "fab": cf.as_dict(), "fb": cb.as_dict()})
+        print(f"# M={M}: overlapped {us_ovl:.3f} us, sequential {us_seq:.3f} us", flush=True)
+        for l in lines[-3:]:
+            print(l, flush=True)
+    pb.plan.close()
+    return lines, dump
+
+
 def table_line(M, N, K, cfg, overlap=1, us=None):
     kind = binding.KIND_NAMES[cfg.kind]
     s = (f"{M} {N} {K} {kind} {cfg.split_k} {cfg.block} {cfg.rows} {cfg.k_unroll} {cfg.producers} "
@@ -162,7 +267,8 @@ def table_line(M, N, K, cfg, overlap=1, us=None):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--shapes", default="kda", help="kda | sweep | N:K[,N:K...]")
+    ap.add_argument("--shapes", default="kda",
+                    help="kda-plan (joint, for the projection) | kda | sweep | N:K[,N:K...]")
     ap.add_argument("--m", type=int, nargs="*", default=None)
     ap.add_argument("--kinds", default="cc,tc05,smallk")
     ap.add_argument("--out", default=None)
@@ -177,6 +283,11 @@ def main(argv=None):
     binding.table_clear()
     dev = torch.device("cuda", torch.cuda.current_device())
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if args.shapes == "kda-plan":
+        ms = args.m or [1, 2, 4, 8, 16, 32, 64, 128]
+        lines, dump = tune_plan(ms, sms, dev, args.v)
+        _write(args, dev, sms, lines, dump)
+        return
     if args.shapes == "kda":
         shapes = KDA_SHAPES
         ms = args.m or [1, 2, 4, 8, 16, 32, 64, 128]
@@ -200,6 +311,10 @@ def main(argv=None):
                          "results": [{"us": us, **c.as_dict()} for us, c in res[:args.top]]})
             print(lines[-1], flush=True)
     print(f"# sweep took {time.time() - t0:.1f} s", file=sys.stderr)
+    _write(args, dev, sms, lines, dump)
+
+
+def _write(args, dev, sms, lines, dump):
     if args.out:
         with open(args.out, "w") as f:
             f.write("# kdaproj autotune table v1 (measured on "
