@@ -1,7 +1,7 @@
 // CUDA-core split-K weight-streaming GEMV for M <= 16 tokens.
 //
 // y[m, n] = bf16( sum_k x[m, k] * W[n, k] ), fp32 accumulation: the skinny
-// GEMM of "[Model] Kimi K3 support part 1" (CuteSkinnyGemm, section
+// GEMM of the Kimi K3 support page, part 1 (vllm PR #50089 digest, CuteSkinnyGemm, section
 // "关键源码片段"), whose design is prior art here: CUDA-core FMAs over 16-byte
 // vector loads, warp-shuffle row reductions, M unrolled at compile time.
 // Differences from that design: the K range is split over blockIdx.y (split-K)

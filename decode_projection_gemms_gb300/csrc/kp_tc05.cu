@@ -1,10 +1,11 @@
 // TMA-fed tcgen05/TMEM cluster split-K kernel for y = bf16(x * W^T), M <= 256.
 //
-// The contraction is the skinny GEMM of "[Model] Kimi K3 support part 1"
-// (CuteSkinnyGemm docstring: C = A * B^T, bf16 in, fp32 accumulate). The
-// tile pipeline follows the Blackwell pattern that "Kimi-K3 GEMM-RS" (vllm PR
-// 52079, section "实现拆解" item 1: TMA loads of A and B, tcgen05 BF16 MMA,
-// mbarrier expect-tx stages) uses as prior art, re-designed for decode, where
+// The contraction is the skinny GEMM of the Kimi K3 support page, part 1
+// (vllm PR #50089 digest, CuteSkinnyGemm docstring: C = A * B^T, bf16 in,
+// fp32 accumulate). The tile pipeline follows the Blackwell pattern of the
+// fused GEMM + reduce-scatter page (vllm PR #52079 digest, section "实现拆解"
+// item 1: TMA loads of A and B, tcgen05 BF16 MMA, mbarrier expect-tx stages),
+// taken as prior art and re-designed for decode, where
 // the whole cost is streaming W once from HBM:
 //
 //  * swap-AB: the MMA's M = 128 rows are output features (rows of W), its N

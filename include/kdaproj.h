@@ -6,7 +6,7 @@
  *     y[m, n] = bf16( sum_k x[m, k] * W[n, k] ),   fp32 accumulation,
  *
  * i.e. C[M,N] = A[M,K] * B[N,K]^T with bf16 inputs, fp32 accumulation and bf16
- * output ("[Model] Kimi K3 support part 1", vllm PR 50089, section
+ * output (Kimi K3 support page, part 1: vllm PR #50089 digest, section
  * "关键源码片段", CuteSkinnyGemm docstring), applied to the Kimi-K3 KDA input
  * projections of one TP8 rank ("[Kimi-K3] Overlap low-M TP8 KDA projections",
  * vllm PR 54697, section "关键源码片段", run_kda_projection_overlap):

@@ -11,8 +11,8 @@
  *   y[m, n] = sum_{k = 0 .. K-1} x[m, k] * W[n, k]           (C = A * B^T)
  *
  * on the bf16 inputs widened exactly to double, summed in ascending k, one
- * output at a time. This is the skinny GEMM of "[Model] Kimi K3 support part 1"
- * (page vllm PR 50089, section "关键源码片段", CuteSkinnyGemm docstring: C[M,N] =
+ * output at a time. This is the skinny GEMM of the Kimi K3 support page, part 1
+ * (vllm PR #50089 digest, section "关键源码片段", CuteSkinnyGemm docstring: C[M,N] =
  * A[M,K] @ B[N,K].T with fp32 accumulation, bf16/fp16 inputs). The oracle uses
  * double instead of fp32 so that its own rounding error is far below the
  * comparison tolerance; the result is left in double.

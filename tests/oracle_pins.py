@@ -2,7 +2,8 @@
 
 Each pin takes an ``oracle.Oracle`` and raises ``AssertionError`` when the
 oracle disagrees with something that the definition ``y = x * W^T`` (skinny
-GEMM docstring of "[Model] Kimi K3 support part 1", CuteSkinnyGemm) and the
+GEMM docstring of the Kimi K3 support page, part 1 (vllm PR #50089 digest,
+CuteSkinnyGemm) and the
 chained projection of "[Kimi-K3] Overlap low-M TP8 KDA projections"
 (run_kda_projection_overlap) fix independently:
 
