@@ -219,13 +219,22 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
         for C in (1, 2, 4, 8, 16):
             for nkb in (2, 4):
                 for stages in (2, 3):
-                    f_cands.append(KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=stages))
+                    for fuse in (0, binding.FLAG_FUSE_FB):
+                        f_cands.append(KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=stages,
+                                                  flags=binding.FLAG_PDL | fuse))
         if M <= 16:
             f_cands += [c for c in cc_candidates(M, pb.Nfab, pb.K, sms) if c.split_k <= 8]
         best = None
-        for (_, cq), (_, cb), cf in itertools.product(q_res, b_res, f_cands):
+        combos = []
+        for (_, cq), cf in itertools.product(q_res, f_cands):
+            # a fused F_A/beta launch computes F_B itself: one F_B candidate is enough
+            for (_, cb) in (b_res[:1] if cf.flags & binding.FLAG_FUSE_FB else b_res):
+                combos.append((cq, cb, cf))
+        for cq, cb, cf in combos:
             try:
-                binding.scratch_bytes(M, pb.Nfab, pb.K, cf, sms)
+                plain = KpCfg.from_buffer_copy(cf)
+                plain.flags &= ~binding.FLAG_FUSE_FB
+                binding.scratch_bytes(M, pb.Nfab, pb.K, plain, sms)
                 pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
                 pb.plan.set_config(binding.BRANCH_FAB, M, cf)
                 pb.plan.set_config(binding.BRANCH_FB, M, cb)

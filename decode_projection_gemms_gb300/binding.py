@@ -27,6 +27,7 @@ STATUS_NAMES = {0: "KP_OK", -1: "KP_EINVAL", -2: "KP_EALIGN", -3: "KP_ESHAPE", -
 KIND_AUTO, KIND_CC, KIND_TC05, KIND_SMALLK = 0, 1, 2, 3
 KIND_NAMES = {0: "auto", 1: "cc", 2: "tc05", 3: "smallk"}
 FLAG_PDL = 1
+FLAG_FUSE_FB = 2
 BRANCH_QKVG, BRANCH_FAB, BRANCH_FB = 0, 1, 2
 
 # exported symbols (must match include/kdaproj.h)

@@ -188,6 +188,8 @@ static cudaError_t launch_gemm(GemmArgs a, const kp_cfg &c, int sms, cudaStream_
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static int check_cfg(int M, int N, int K, const kp_cfg &c) {
+    if (c.flags & KP_FLAG_FUSE_FB)
+        return set_error(KP_ECONFIG, "KP_FLAG_FUSE_FB applies only to the F_A/beta branch of a plan");
     if (c.kind == KP_KIND_CC && M > 16)
         return set_error(KP_ECONFIG, "CUDA-core kernel supports M <= 16 (got M=%d)", M);
     if (!cfg_supported(M, N, K, c))
@@ -220,6 +222,22 @@ namespace kp {
 struct BranchShape {
     int N, K;
 };
+
+// Validation of a configuration for one branch of a plan: the F_A/beta
+// branch may carry KP_FLAG_FUSE_FB (tcgen05 kernel, F_A = its first 128 rows).
+static int check_branch_cfg(int branch, int M, int N, int K, const kp_cfg &c) {
+    if (!(c.flags & KP_FLAG_FUSE_FB)) return check_cfg(M, N, K, c);
+    if (branch != KP_BRANCH_FAB)
+        return set_error(KP_ECONFIG, "KP_FLAG_FUSE_FB applies only to the F_A/beta branch");
+    kp_cfg plain = c;
+    plain.flags &= ~KP_FLAG_FUSE_FB;
+    int rc = check_cfg(M, N, K, plain);
+    if (rc) return rc;
+    if (c.kind != KP_KIND_TC05 || (M <= 256 && !tc05_fusable(M, c)))
+        return set_error(KP_ECONFIG,
+                         "KP_FLAG_FUSE_FB needs the tcgen05 kernel with room for the F_B operands");
+    return KP_OK;
+}
 
 static BranchShape branch_shape(const kda_plan *p, int b) {
     if (b == KP_BRANCH_QKVG) return {p->Nq, p->K};
@@ -345,6 +363,7 @@ int skinny_gemm(const void *x, const void *W, void *y, int M, int N, int K, cons
         if ((rc = check_cfg(M, N, K, c))) return rc;
     } else {
         c = select_config(M, N, K, d->sms, nullptr);
+        c.flags &= ~KP_FLAG_FUSE_FB;  // a plan-only flag in a table entry
         if (cfg) c.flags = cfg->flags | (c.flags & ~KP_FLAG_PDL);
         if ((rc = check_cfg(M, N, K, c))) return rc;
     }
@@ -425,7 +444,11 @@ int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_plan **
         for (int M = 1; M <= max_M; ++M) {
             int ov = 1;
             kp_cfg c = select_config(M, sh.N, sh.K, p->sms, &ov);
-            if ((rc = check_cfg(M, sh.N, sh.K, c))) {
+            if (c.flags & KP_FLAG_FUSE_FB) {
+                // a fused table entry that does not fit this branch: drop the fusion
+                if (check_branch_cfg(b, M, sh.N, sh.K, c) != KP_OK) c.flags &= ~KP_FLAG_FUSE_FB;
+            }
+            if ((rc = check_branch_cfg(b, M, sh.N, sh.K, c))) {
                 delete p;
                 return rc;
             }
@@ -484,7 +507,7 @@ int kda_proj_set_config(kda_plan *plan, int branch, int M, const kp_cfg *cfg) {
     if (!cfg || branch < 0 || branch > 2 || M < 1 || M > plan->max_M)
         return set_error(KP_EINVAL, "kda_proj_set_config: bad argument");
     const BranchShape sh = branch_shape(plan, branch);
-    int rc = check_cfg(M, sh.N, sh.K, *cfg);
+    int rc = check_branch_cfg(branch, M, sh.N, sh.K, *cfg);
     if (rc) return rc;
     Scratch s = scratch_of(M, sh.N, sh.K, *cfg, plan->sms);
     if (s.floats > plan->ws_floats[branch] || s.counters > plan->cnt_n[branch])
@@ -556,22 +579,40 @@ int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, cons
     cudaStream_t ms = main_stream;
     cudaStream_t side = overlap ? static_cast<cudaStream_t>(aux_stream) : ms;
 
+    // F_A/beta, then F_B: one fused launch when the F_A/beta configuration
+    // carries KP_FLAG_FUSE_FB (the F_A tile's cluster computes F_B), else two.
+    const bool fuse = cf.kind == KP_KIND_TC05 && (cf.flags & KP_FLAG_FUSE_FB) && M <= 256;
+    auto launch_aux = [&](cudaStream_t st) -> cudaError_t {
+        kp_cfg c = cf;
+        c.flags &= ~KP_FLAG_FUSE_FB;
+        if (fuse) {
+            FusedFB fb;
+            fb.W = g.W;
+            fb.N = g.N;
+            fb.y = g.y;
+            fb.ld = g.ldy;
+            fb.tile = 0;
+            return tc05_launch(f, c, plan->sms, st, &fb);
+        }
+        cudaError_t e2 = launch_gemm(f, c, plan->sms, st);
+        if (e2 != cudaSuccess) return e2;
+        return launch_gemm(g, cb, plan->sms, st);
+    };
+
     if (overlap) {
         if ((e = cudaEventRecord(events[0], ms)) != cudaSuccess) return cuda_fail(e, "fork: cudaEventRecord");
         if ((e = cudaStreamWaitEvent(side, events[0], 0)) != cudaSuccess)
             return cuda_fail(e, "fork: cudaStreamWaitEvent");
         // aux branch first, so its small grids are dispatched before the
         // main-stream kernel spreads over every SM
-        if ((e = launch_gemm(f, cf, plan->sms, side)) != cudaSuccess) return cuda_fail(e, "F_A/beta launch");
-        if ((e = launch_gemm(g, cb, plan->sms, side)) != cudaSuccess) return cuda_fail(e, "F_B launch");
+        if ((e = launch_aux(side)) != cudaSuccess) return cuda_fail(e, "F_A/beta -> F_B launch");
         if ((e = cudaEventRecord(events[1], side)) != cudaSuccess) return cuda_fail(e, "join: cudaEventRecord");
         if ((e = launch_gemm(q, cq, plan->sms, ms)) != cudaSuccess) return cuda_fail(e, "QKVG launch");
         if ((e = cudaStreamWaitEvent(ms, events[1], 0)) != cudaSuccess)
             return cuda_fail(e, "join: cudaStreamWaitEvent");
     } else {
         if ((e = launch_gemm(q, cq, plan->sms, ms)) != cudaSuccess) return cuda_fail(e, "QKVG launch");
-        if ((e = launch_gemm(f, cf, plan->sms, ms)) != cudaSuccess) return cuda_fail(e, "F_A/beta launch");
-        if ((e = launch_gemm(g, cb, plan->sms, ms)) != cudaSuccess) return cuda_fail(e, "F_B launch");
+        if ((e = launch_aux(ms)) != cudaSuccess) return cuda_fail(e, "F_A/beta -> F_B launch");
     }
     return KP_OK;
 }

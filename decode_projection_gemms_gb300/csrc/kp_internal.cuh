@@ -36,10 +36,22 @@ bool cc_supported(int M, int K, const kp_cfg &c);
 Scratch cc_scratch(int M, int N, int K, const kp_cfg &c);
 cudaError_t cc_launch(const GemmArgs &a, const kp_cfg &c, cudaStream_t s);
 
-// tcgen05 stream-K kernel (kp_tc05.cu)
+// F_B fused into the F_A/beta launch: tile `tile` of that GEMM holds the 128
+// F_A rows; y = bf16(bf16(F_A) * W^T) with W [N, 128].
+struct FusedFB {
+    const __nv_bfloat16 *W;
+    int N;
+    __nv_bfloat16 *y;
+    int64_t ld;
+    int tile;
+};
+
+// tcgen05 cluster split-K kernel (kp_tc05.cu)
 bool tc05_supported(int M, int N, int K, const kp_cfg &c);
+bool tc05_fusable(int M, const kp_cfg &c);
 Scratch tc05_scratch(int M, int N, int K, const kp_cfg &c, int num_sms);
-cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStream_t s);
+cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStream_t s,
+                        const FusedFB *fb = nullptr);
 int tc05_max_stages(int M);
 kp_cfg tc05_default(int M, int N, int K, int num_sms);
 

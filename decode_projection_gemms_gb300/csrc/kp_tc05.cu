@@ -53,7 +53,7 @@ constexpr int kTileN = 128;            // features per tile (UMMA M)
 constexpr int kBlockK = 64;            // K elements per block (128 bytes)
 constexpr uint32_t kWBlockBytes = kTileN * kBlockK * 2;  // 16 KB per K block
 constexpr int kMaxSmem = 227 * 1024;
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
 
 struct Tc05Params {
     __nv_bfloat16 *y;
@@ -66,6 +66,15 @@ struct Tc05Params {
     int x3d;           // 1: x of a full stage is one 3-D box (K % 64 == 0)
     int producers;     // warps issuing TMA copies (1..5)
     int stages;
+    // Fused F_B: the CTAs of tile `fb_tile` (whose 128 rows are F_A) also
+    // compute yfb = bf16(bf16(F_A) * W_fb^T); -1 = no fusion.
+    int fb_tile;
+    int fb_tiles;      // 128-row tiles of W_fb
+    int N_fb;
+    __nv_bfloat16 *yfb;
+    int64_t ldfb;
+    uint32_t off_bfa;  // shared-memory offset of the F_A operand [2][Mpad][128 B]
+    uint32_t off_wfb;  // shared-memory offset of one W_fb tile [2][128][128 B]
     uint32_t idesc;
     uint32_t tmem_cols;
     uint32_t stage_bytes;
@@ -80,6 +89,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo) {
            (static_cast<uint64_t>(2) << 61);
 }
 
+// Byte offset of element (token m, feature k) of the fused F_B's B operand:
+// K-major, 128-byte swizzle, two 64-wide K blocks of Mpad rows x 128 bytes.
+__device__ __forceinline__ uint32_t bfa_offset(int m, int k, int Mpad) {
+    return static_cast<uint32_t>((k >> 6) * Mpad * 128 + m * 128 +
+                                 ((((k & 63) >> 3) ^ (m & 7)) << 4) + (k & 7) * 2);
+}
+
 // Wait (bounded by time only) for a barrier phase; used to drain copies.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
@@ -89,7 +105,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc05_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
-                const __grid_constant__ CUtensorMap tmx3, const Tc05Params p) {
+                const __grid_constant__ CUtensorMap tmx3, const __grid_constant__ CUtensorMap tmfb,
+                const Tc05Params p) {
     extern __shared__ uint8_t tc_smem_raw[];
     const uint32_t raw = smem_u32(tc_smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -99,7 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(gbase + static_cast<size_t>(S) * p.stage_bytes);
     uint64_t *empty = full + S;
     uint64_t *accf = empty + S;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accf + 1);
+    uint64_t *fbw = accf + 1;      // fused F_B: W_fb tile landed
+    uint64_t *fbacc = fbw + 1;     // fused F_B: accumulator ready
+    uint64_t *fbempty = fbacc + 1; // fused F_B: accumulator drained
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fbempty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -110,6 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kb0 = static_cast<int>((static_cast<long long>(p.KB) * rank) / C);
     const int kb1 = static_cast<int>((static_cast<long long>(p.KB) * (rank + 1)) / C);
     const int n_st = (kb1 - kb0 + p.nkb - 1) / p.nkb;  // stages of work for this CTA
+    const bool fused = (p.fb_tile >= 0 && tile == p.fb_tile);
+    // fused F_B tiles of this CTA: rank, rank + C, ...
+    const int my_fb = fused && rank < p.fb_tiles ? (p.fb_tiles - rank + C - 1) / C : 0;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) {
@@ -117,11 +140,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(empty + s), 1);
         }
         mbar_init(smem_u32(accf), 1);
+        mbar_init(smem_u32(fbw), 1);
+        mbar_init(smem_u32(fbacc), 1);
+        mbar_init(smem_u32(fbempty), 4);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmw);
         tma_prefetch_desc(&tmx);
         if (p.x3d) tma_prefetch_desc(&tmx3);
+        if (fused) tma_prefetch_desc(&tmfb);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
@@ -191,6 +218,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = first; s < n_st; ++s)
                 drain_wait(smem_u32(full + (s % S)), static_cast<uint32_t>((s / S) & 1));
         }
+        if (pidx == 0 && my_fb > 0) {
+            // The pipeline memory is free once every main-loop MMA has
+            // completed: fetch this CTA's first W_fb tile while the epilogue
+            // and the cluster reduction run.
+            mbar_wait_bounded(smem_u32(accf), 0, abort_flag, p.err, DEV_TIMEOUT_ACC_FULL);
+            const uint32_t dst = base + p.off_wfb;
+            mbar_expect_tx(smem_u32(fbw), 2 * kWBlockBytes);
+            for (int j = 0; j < 2; ++j)
+                tma_load_2d(dst + j * kWBlockBytes, &tmfb, smem_u32(fbw), j * kBlockK,
+                            rank * kTileN, policy_evict_last());
+        }
     }
     if (warp == 0) {
         // lanes 1..31 of warp 0 have nothing to do until the end
@@ -239,7 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (m < p.M) {
                     const float f = __uint_as_float(v[i]);
                     if (C == 1) {
-                        if (n < p.N) p.y[m * p.ldy + n] = __float2bfloat16_rn(f);
+                        const __nv_bfloat16 b = __float2bfloat16_rn(f);
+                        if (n < p.N) p.y[m * p.ldy + n] = b;
+                        if (fused)
+                            *reinterpret_cast<__nv_bfloat16 *>(gbase + p.off_bfa +
+                                                              bfa_offset(m, row, p.Mpad)) = b;
                     } else {
                         red[m * kTileN + row] = f;
                     }
@@ -276,13 +318,111 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             const int nb = tile * kTileN + rr;
             __nv_bfloat16 *yr = p.y + m * p.ldy;
-            if (nb + 0 < p.N) yr[nb + 0] = __float2bfloat16_rn(acc.x);
-            if (nb + 1 < p.N) yr[nb + 1] = __float2bfloat16_rn(acc.y);
-            if (nb + 2 < p.N) yr[nb + 2] = __float2bfloat16_rn(acc.z);
-            if (nb + 3 < p.N) yr[nb + 3] = __float2bfloat16_rn(acc.w);
+            const __nv_bfloat16 b0 = __float2bfloat16_rn(acc.x);
+            const __nv_bfloat16 b1 = __float2bfloat16_rn(acc.y);
+            const __nv_bfloat16 b2 = __float2bfloat16_rn(acc.z);
+            const __nv_bfloat16 b3 = __float2bfloat16_rn(acc.w);
+            if (nb + 0 < p.N) yr[nb + 0] = b0;
+            if (nb + 1 < p.N) yr[nb + 1] = b1;
+            if (nb + 2 < p.N) yr[nb + 2] = b2;
+            if (nb + 3 < p.N) yr[nb + 3] = b3;
+            if (fused) {
+                // this rank's features rr..rr+3 of the F_B operand (8 bytes)
+                __nv_bfloat162 lo, hi;
+                lo.x = b0; lo.y = b1; hi.x = b2; hi.y = b3;
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t *>(&lo);
+                pk.y = *reinterpret_cast<uint32_t *>(&hi);
+                *reinterpret_cast<uint2 *>(gbase + p.off_bfa + bfa_offset(m, rr, p.Mpad)) = pk;
+            }
         }
         // Peers may still be reading this CTA's partial tile.
         cluster_sync_all();
+        if (fused) {
+            // Gather the other ranks' F_A features (16-byte chunks of 8).
+            const int cpr = rpc / 8;  // chunks per rank
+            const int gather = my_fb > 0 ? p.M * 16 : 0;
+            for (int idx = threadIdx.x; idx < gather; idx += kThreads) {
+                const int m = idx >> 4;
+                const int c = idx & 15;
+                const int owner = c / cpr;
+                if (owner == rank) continue;
+                const uint32_t off = base + p.off_bfa + bfa_offset(m, c * 8, p.Mpad);
+                uint4 v;
+                asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                             : "r"(mapa_shared(off, static_cast<uint32_t>(owner)))
+                             : "memory");
+                *reinterpret_cast<uint4 *>(gbase + p.off_bfa + bfa_offset(m, c * 8, p.Mpad)) = v;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // everyone has copied everything it needs from its peers
+            cluster_sync_all();
+        }
+    } else if (fused) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        tc_fence_before();
+        __syncthreads();
+    }
+
+    if (my_fb > 0) {
+        // ---------------- fused F_B: out_fb = bf16(F_A) * W_fb^T ----------------
+        const uint32_t a_base = base + p.off_wfb;
+        const uint32_t b_base = base + p.off_bfa;
+        if (warp == 0 && lane == 0) {
+            for (int i = 1; i < my_fb; ++i) {
+                mbar_wait_bounded(smem_u32(fbacc), static_cast<uint32_t>((i - 1) & 1), abort_flag,
+                                  p.err, DEV_TIMEOUT_ACC_FULL);
+                mbar_expect_tx(smem_u32(fbw), 2 * kWBlockBytes);
+                for (int j = 0; j < 2; ++j)
+                    tma_load_2d(a_base + j * kWBlockBytes, &tmfb, smem_u32(fbw), j * kBlockK,
+                                (rank + i * C) * kTileN, policy_evict_last());
+            }
+        } else if (warp == 1 && lane == 0) {
+            tc_fence_after();
+            for (int i = 0; i < my_fb; ++i) {
+                if (i > 0)
+                    mbar_wait_bounded(smem_u32(fbempty), static_cast<uint32_t>((i - 1) & 1),
+                                      abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY);
+                mbar_wait_bounded(smem_u32(fbw), static_cast<uint32_t>(i & 1), abort_flag, p.err,
+                                  DEV_TIMEOUT_FULL);
+                tc_fence_after();
+                for (int j = 0; j < 2; ++j) {
+                    const uint64_t ad = smem_desc(a_base + j * kWBlockBytes, 1024);
+                    const uint64_t bd = smem_desc(b_base + j * p.Mpad * 128, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk)
+                        umma_bf16(tmem_base, ad + 2 * kk, bd + 2 * kk, p.idesc,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                umma_commit(smem_u32(fbacc));
+            }
+        } else if (warp >= 2) {
+            const int q = warp & 3;
+            const int row = q * 32 + lane;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            for (int i = 0; i < my_fb; ++i) {
+                mbar_wait_bounded(smem_u32(fbacc), static_cast<uint32_t>(i & 1), abort_flag, p.err,
+                                  DEV_TIMEOUT_ACC_FULL);
+                tc_fence_after();
+                const int n = (rank + i * C) * kTileN + row;
+                for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int m = c0 + e;
+                        if (m < p.M && n < p.N_fb)
+                            p.yfb[m * p.ldfb + n] = __float2bfloat16_rn(__uint_as_float(v[e]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(fbempty));
+            }
+        }
     }
 
     tc_fence_before();
@@ -426,9 +566,33 @@ bool tc05_supported(int M, int N, int K, const kp_cfg &c) {
 
 Scratch tc05_scratch(int, int, int, const kp_cfg &, int) { return Scratch(); }
 
-cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStream_t stream) {
+namespace {
+// Shared-memory layout of the fused F_B after the main loop (offsets from the
+// 1024-aligned base): [partial tile Mpad x 128 fp32][F_A operand 2 x Mpad x
+// 128 B][one W_fb tile 2 x 16 KB]. It must fit in the pipeline memory.
+void fb_layout(int Mpad, uint32_t *off_bfa, uint32_t *off_wfb, uint32_t *end) {
+    auto al = [](uint32_t v) { return (v + 1023u) & ~1023u; };
+    *off_bfa = al(static_cast<uint32_t>(Mpad) * kTileN * 4);
+    *off_wfb = al(*off_bfa + static_cast<uint32_t>(Mpad) * 256);
+    *end = *off_wfb + 2 * kWBlockBytes;
+}
+}  // namespace
+
+bool tc05_fusable(int M, const kp_cfg &c) {
+    if (M < 1 || M > 256) return false;
+    const int Mpad = mpad_of(M);
+    const int nkb = nkb_of(c);
+    const int st = c.stages ? c.stages : max_stages(Mpad, nkb);
+    uint32_t ob, ow, end;
+    fb_layout(Mpad, &ob, &ow, &end);
+    return end <= static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb);
+}
+
+cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStream_t stream,
+                        const FusedFB *fb) {
     (void)num_sms;
     if (!tc05_supported(a.M, a.N, a.K, c)) return cudaErrorInvalidValue;
+    if (fb && !tc05_fusable(a.M, c)) return cudaErrorInvalidValue;
     const int Mpad = mpad_of(a.M);
     const int nkb = nkb_of(c);
     const int stages = c.stages ? c.stages : max_stages(Mpad, nkb);
@@ -451,6 +615,25 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.tmem_cols = tmem_cols_of(Mpad);
     p.stage_bytes = stage_bytes_of(Mpad, nkb);
     p.w_stage_bytes = w_stage_bytes_of(nkb);
+    p.fb_tile = -1;
+    p.fb_tiles = 0;
+    p.N_fb = 0;
+    p.yfb = nullptr;
+    p.ldfb = 0;
+    p.off_bfa = p.off_wfb = 0;
+    CUtensorMap mfb;
+    memset(&mfb, 0, sizeof mfb);
+    if (fb) {
+        uint32_t end;
+        fb_layout(Mpad, &p.off_bfa, &p.off_wfb, &end);
+        p.fb_tile = fb->tile;
+        p.N_fb = fb->N;
+        p.fb_tiles = (fb->N + kTileN - 1) / kTileN;
+        p.yfb = fb->y;
+        p.ldfb = fb->ld;
+        cudaError_t e2 = make_map(&mfb, fb->W, fb->N, kTileN, kTileN, kTileN);
+        if (e2 != cudaSuccess) return e2;
+    }
 
     CUtensorMap mw, mx, mx3;
     cudaError_t e = make_map(&mw, a.W, a.N, a.K, a.K, kTileN);
@@ -497,7 +680,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, tc05_kernel, mw, mx, mx3, p);
+    return cudaLaunchKernelEx(&cfg, tc05_kernel, mw, mx, mx3, mfb, p);
 }
 
 }  // namespace kp

@@ -87,10 +87,13 @@ enum kp_kind {
 };
 
 enum kp_flags {
-    KP_FLAG_PDL = 1 /* launch with programmatic stream serialisation: the
-                       kernel may start (and stream its weights) while the
-                       previous kernel on the stream finishes; it waits for
-                       that kernel before touching x, y or scratch */
+    KP_FLAG_PDL = 1,    /* launch with programmatic stream serialisation: the
+                           kernel may start (and stream its weights) while the
+                           previous kernel on the stream finishes; it waits for
+                           that kernel before touching x, y or scratch */
+    KP_FLAG_FUSE_FB = 2 /* F_A/beta branch of kda_proj_run only (TC05 kind,
+                           M <= 256): the F_A/beta launch also computes F_B
+                           from its bf16 F_A tile, so the F_B launch is skipped */
 };
 
 /* One kernel configuration. Fields a kind does not use are ignored. */

@@ -142,6 +142,14 @@ def test_scratch_sizes(lib):
     assert e.value.code == binding.KP_ECONFIG
 
 
+def test_fuse_flag_is_plan_only(lib):
+    fused = binding.KpCfg.make("tc05", split_k=4, k_unroll=2,
+                               flags=binding.FLAG_PDL | binding.FLAG_FUSE_FB)
+    with pytest.raises(binding.KdaProjError) as e:
+        binding.scratch_bytes(4, 136, 7168, fused, 152)
+    assert e.value.code == binding.KP_ECONFIG
+
+
 def test_missing_library_fails_loudly(tmp_path):
     saved = binding._lib
     binding._lib = None

@@ -302,6 +302,70 @@ def test_overlap_graph_pdl_bit_identical(plan, M):
         plan.set_overlap(-1)
 
 
+# ---- F_B fused into the F_A/beta launch ------------------------------------------------------
+
+FUSED_FAB = [KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=st,
+                        flags=binding.FLAG_PDL | binding.FLAG_FUSE_FB)
+             for (C, nkb, st) in ((1, 2, 0), (2, 4, 2), (4, 2, 3), (8, 4, 2), (16, 2, 0))]
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 64, 128, 200])
+@pytest.mark.parametrize("ci", range(len(FUSED_FAB)))
+def test_kda_fused_fb(plan, M, ci):
+    cf = FUSED_FAB[ci]
+    saved = plan.get_config(binding.BRANCH_FAB, M)
+    try:
+        plan.set_config(binding.BRANCH_FAB, M, cf)
+    except binding.KdaProjError as e:
+        assert e.code == binding.KP_ECONFIG   # no room for the F_B operands at this M
+        pytest.skip(str(e))
+    x, wp, wfb = kda_inputs(M, layer=3, seed=5)
+    x, wp, wfb = x.cuda(), wp.cuda(), wfb.cuda()
+    aux = torch.cuda.Stream()
+    evs = binding.make_events()
+    try:
+        seq = _run(plan, x, wp, wfb, False, aux, evs)
+        ovl = _run(plan, x, wp, wfb, True, aux, evs)
+        for a, b in zip(seq, ovl):
+            assert torch.equal(a, b)
+        check_kda(ovl, x.cpu(), wp.cpu(), wfb.cpu(), 4096, 136, f"fused C={cf.split_k} M={M}")
+        # the fused F_B runs the same MMA sequence as the tcgen05 kernel with
+        # one CTA per tile on the bf16 F_A: bit-identical
+        ref_fb = binding.skinny_gemm(ovl[1][:, :128].contiguous(), wfb,
+                                     cfg=KpCfg.make("tc05", split_k=1, k_unroll=2))
+        torch.cuda.synchronize()
+        assert torch.equal(ref_fb, ovl[2])
+    finally:
+        plan.set_config(binding.BRANCH_FAB, M, saved)
+        plan.set_overlap(-1)
+
+
+def test_kda_fused_fb_graph_replay(plan):
+    M = 8
+    cf = FUSED_FAB[3]
+    saved = plan.get_config(binding.BRANCH_FAB, M)
+    plan.set_config(binding.BRANCH_FAB, M, cf)
+    x, wp, wfb = kda_inputs(M, layer=4, seed=6)
+    x, wp, wfb = x.cuda(), wp.cuda(), wfb.cuda()
+    aux = torch.cuda.Stream()
+    evs = binding.make_events()
+    try:
+        seq = _run(plan, x, wp, wfb, False, aux, evs)
+        outs = (poisoned((M, 4096)), poisoned((M, 136)), poisoned((M, 1024)))
+        plan.set_overlap(1)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.run(x, wp, wfb, *outs, aux_stream=aux, events=evs)
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(seq, outs):
+            assert torch.equal(a, b)
+    finally:
+        plan.set_config(binding.BRANCH_FAB, M, saved)
+        plan.set_overlap(-1)
+
+
 # ---- boundary errors on a live device -------------------------------------------------------
 
 def test_errors_on_device(plan):
