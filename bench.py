@@ -39,9 +39,9 @@ K, N_QKVG, N_FAB, N_FA, N_FB = 7168, 4096, 136, 128, 1024
 LAYERS = 48
 METRIC = "KDA proj µs/call and HBM GB/s (% of ~8 TB/s) at M=1..128, bf16, 1×GB300"
 UNIT = "us/call"
-WORKLOAD = ("full overlapped KDA decode projection: packed [4096+136, 7168] bf16 + W_fb [1024,128] "
-            "bf16, QKVG on main stream || F_A/beta->F_B (PDL) on aux stream, graph-replayed, "
-            "48-layer weight stack rotated per call")
+WORKLOAD = ("full KDA decode projection: packed [4096+136, 7168] bf16 + W_fb [1024,128] bf16; "
+            "QKVG || F_A/beta->F_B (per-M mode from the table: two-stream overlap or one launch), "
+            "graph-replayed, 48-layer weight stack rotated per call")
 
 
 def call_bytes(M: int) -> int:
@@ -225,6 +225,7 @@ def run_ours(args):
     graphs = {M: capture(M, -1) for M in m_list}
     graphs_seq = {M: capture(M, 0) for M in m_list}
     graphs_ovl = {M: capture(M, 1) for M in m_list}
+    graphs_one = {M: capture(M, 2) for M in m_list}
     graphs_q = {M: capture(M, -1, qkvg_only=True) for M in m_list}
 
     def timed(gs, steps):
@@ -264,6 +265,7 @@ def run_ours(args):
         tot, wall_ms = timed(graphs, args.steps)
         tot_seq, _ = timed(graphs_seq, args.cmp_steps)
         tot_ovl, _ = timed(graphs_ovl, args.cmp_steps)
+        tot_one, _ = timed(graphs_one, args.cmp_steps)
         tot_q, _ = timed(graphs_q, args.cmp_steps)
     e2e = run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist)
     clock_info = clocks.stop()
@@ -271,19 +273,22 @@ def run_ours(args):
     # reductions (max over ranks)
     keys = list(m_list)
     vals = reduce_max([tot[M] for M in keys] + [tot_seq[M] for M in keys] +
-                      [tot_ovl[M] for M in keys] + [tot_q[M] for M in keys] + [wall_ms], dist)
+                      [tot_ovl[M] for M in keys] + [tot_one[M] for M in keys] +
+                      [tot_q[M] for M in keys] + [wall_ms], dist)
     nM = len(keys)
     tot = dict(zip(keys, vals[0:nM]))
     tot_seq = dict(zip(keys, vals[nM:2 * nM]))
     tot_ovl = dict(zip(keys, vals[2 * nM:3 * nM]))
-    tot_q = dict(zip(keys, vals[3 * nM:4 * nM]))
-    wall_ms = vals[4 * nM]
+    tot_one = dict(zip(keys, vals[3 * nM:4 * nM]))
+    tot_q = dict(zip(keys, vals[4 * nM:5 * nM]))
+    wall_ms = vals[5 * nM]
 
     per_m = {}
     for M in keys:
         us = tot[M] * 1e3 / (args.steps * L)
         us_seq = tot_seq[M] * 1e3 / (args.cmp_steps * L)
         us_ovl = tot_ovl[M] * 1e3 / (args.cmp_steps * L)
+        us_one = tot_one[M] * 1e3 / (args.cmp_steps * L)
         us_q = tot_q[M] * 1e3 / (args.cmp_steps * L)
         roof_us = max(call_bytes(M) / (hbm_peak * 1e3), call_flops(M) / (tc_peak * 1e6))
         per_m[str(M)] = {
@@ -292,9 +297,10 @@ def run_ours(args):
             "roofline_us": round(roof_us, 3),
             "frac_of_roofline": round(roof_us / us, 4),
             "frac_of_8tbs": round(call_bytes(M) / (us * 1e3) / 8000.0, 4),
-            "overlap": bool(plan.overlap_at(M)),
+            "mode": {0: "sequential", 1: "overlapped", 2: "single-launch"}[plan.overlap_at(M)],
             "us_sequential": round(us_seq, 3),
             "us_overlapped": round(us_ovl, 3),
+            "us_single_launch": round(us_one, 3),
             "overlap_speedup": round(us_seq / us_ovl, 4),
             "qkvg_kernel_us": round(us_q, 3),
             "qkvg_kernel_gbs": round(qkvg_bytes(M) / (us_q * 1e3), 1),

@@ -254,13 +254,41 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
         pb.plan.set_config(binding.BRANCH_FB, M, cb)
         us_ovl = pb.time_call(M, 1)
         us_seq = pb.time_call(M, 0)
-        ov = 1 if us_ovl < us_seq else 0
-        lines += [table_line(M, pb.Nq, pb.K, cq, ov, us_ovl),
+        # single launch over the packed weight with the best tcgen05 configs
+        us_one, c_one = None, None
+        for cand in [c for _, c in q_res if c.kind == binding.KIND_TC05] + tc05_candidates(
+                M, pb.Nq + pb.Nfab, pb.K, sms):
+            try:
+                pb.plan.set_config(binding.BRANCH_QKVG, M, cand)
+            except binding.KdaProjError:
+                continue
+            us = pb.time_call(M, 2)
+            if verbose:
+                print(f"  M={M} single launch {us:8.3f} us  {cand.as_dict()}", file=sys.stderr)
+            if us_one is None or us < us_one:
+                us_one, c_one = us, cand
+        # decide between the modes on longer re-measurements (single runs of
+        # 9-layer graphs differ by a few percent)
+        pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
+        times = {0: pb.time_call(M, 0, reps=30, trials=5), 1: pb.time_call(M, 1, reps=30, trials=5)}
+        if us_one is not None:
+            pb.plan.set_config(binding.BRANCH_QKVG, M, c_one)
+            times[2] = pb.time_call(M, 2, reps=30, trials=5)
+            pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
+        us_seq, us_ovl = times[0], times[1]
+        us_one = times.get(2)
+        ov = min(times, key=times.get)
+        if ov == 2:
+            cq = c_one
+        pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
+        lines += [table_line(M, pb.Nq, pb.K, cq, ov, times[ov]),
                   table_line(M, pb.Nfab, pb.K, cf, ov),
                   table_line(M, pb.Nfb, 128, cb, ov)]
         dump.append({"M": M, "overlapped_us": us_ovl, "sequential_us": us_seq,
+                     "single_launch_us": us_one, "mode": ov,
                      "qkvg": cq.as_dict(), "fab": cf.as_dict(), "fb": cb.as_dict()})
-        print(f"# M={M}: overlapped {us_ovl:.3f} us, sequential {us_seq:.3f} us", flush=True)
+        print(f"# M={M}: overlapped {us_ovl:.3f} us, sequential {us_seq:.3f} us, single launch "
+              f"{us_one} us -> mode {ov}", flush=True)
         for l in lines[-3:]:
             print(l, flush=True)
     pb.plan.close()

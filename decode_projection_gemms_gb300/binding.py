@@ -223,8 +223,9 @@ class KdaPlan:
     def set_overlap(self, mode: int):
         _check(self._lib.kda_proj_set_overlap(self._h, int(mode)))
 
-    def overlap_at(self, M: int) -> bool:
-        return bool(self._lib.kda_proj_overlap_at(self._h, M))
+    def overlap_at(self, M: int) -> int:
+        """Mode at M: 0 sequential, 1 overlapped, 2 single launch."""
+        return int(self._lib.kda_proj_overlap_at(self._h, M))
 
     def get_config(self, branch: int, M: int) -> KpCfg:
         c = KpCfg()

@@ -223,6 +223,16 @@ struct BranchShape {
     int N, K;
 };
 
+static BranchShape branch_shape(const kda_plan *p, int b);
+
+// Whether the plan can run the whole projection as one launch at M with the
+// Q/K/V/G configuration c: tcgen05 kernel, F_A rows starting on a 128-row
+// tile, room for the fused F_B operands, no M slicing.
+static bool single_launch_ok(const kda_plan *p, int M, const kp_cfg &c) {
+    return c.kind == KP_KIND_TC05 && M <= 256 && p->Nq % 128 == 0 &&
+           tc05_supported(M, p->Nq + p->Nfab, p->K, c) && tc05_fusable(M, c);
+}
+
 // Validation of a configuration for one branch of a plan: the F_A/beta
 // branch may carry KP_FLAG_FUSE_FB (tcgen05 kernel, F_A = its first 128 rows).
 static int check_branch_cfg(int branch, int M, int N, int K, const kp_cfg &c) {
@@ -453,7 +463,7 @@ int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_plan **
                 return rc;
             }
             p->cfg[b][M] = c;
-            if (b == KP_BRANCH_QKVG) p->overlap[M] = static_cast<uint8_t>(ov != 0);
+            if (b == KP_BRANCH_QKVG) p->overlap[M] = static_cast<uint8_t>(ov < 0 ? 0 : ov > 2 ? 1 : ov);
             Scratch s = scratch_of(M, sh.N, sh.K, c, p->sms);
             if (s.floats > need[b].floats) need[b].floats = s.floats;
             if (s.counters > need[b].counters) need[b].counters = s.counters;
@@ -483,7 +493,7 @@ int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_plan **
 
 int kda_proj_set_overlap(kda_plan *plan, int mode) {
     if (!plan) return set_error(KP_ENOPLAN, "kda_proj_set_overlap: NULL plan");
-    if (mode < -1 || mode > 1) return set_error(KP_EINVAL, "kda_proj_set_overlap: mode %d", mode);
+    if (mode < -1 || mode > 2) return set_error(KP_EINVAL, "kda_proj_set_overlap: mode %d", mode);
     plan->overlap_mode = mode;
     return KP_OK;
 }
@@ -536,8 +546,8 @@ int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, cons
         return set_error(KP_EINVAL, "kda_proj_run: current device %d is not the plan's device %d",
                          dev, plan->dev);
 
-    const bool overlap = kda_proj_overlap_at(plan, M) && aux_stream && events && events[0] &&
-                         events[1];
+    const int mode = kda_proj_overlap_at(plan, M);
+    const bool overlap = mode == 1 && aux_stream && events && events[0] && events[1];
     const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(x);
     const __nv_bfloat16 *wp = static_cast<const __nv_bfloat16 *>(W_packed);
 
@@ -578,6 +588,29 @@ int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, cons
     const kp_cfg &cb = plan->cfg[KP_BRANCH_FB][M];
     cudaStream_t ms = main_stream;
     cudaStream_t side = overlap ? static_cast<cudaStream_t>(aux_stream) : ms;
+
+    if (mode == 2 && single_launch_ok(plan, M, cq)) {
+        // One tcgen05 launch over the packed weight: rows [0, N_qkvg) go to
+        // out_qkvg, the rest to out_fab, and the F_A tile's cluster computes
+        // F_B. Q/K/V/G and F_A/beta tiles run side by side on the SMs.
+        GemmArgs a = q;
+        a.N = plan->Nq + plan->Nfab;
+        SplitOut so;
+        so.n_split = plan->Nq;
+        so.y2 = f.y;
+        so.ldy2 = f.ldy;
+        FusedFB fb;
+        fb.W = g.W;
+        fb.N = g.N;
+        fb.y = g.y;
+        fb.ld = g.ldy;
+        fb.tile = plan->Nq / 128;
+        kp_cfg c = cq;
+        c.flags &= ~KP_FLAG_FUSE_FB;
+        if ((e = tc05_launch(a, c, plan->sms, ms, &fb, &so)) != cudaSuccess)
+            return cuda_fail(e, "single-launch projection");
+        return KP_OK;
+    }
 
     // F_A/beta, then F_B: one fused launch when the F_A/beta configuration
     // carries KP_FLAG_FUSE_FB (the F_A tile's cluster computes F_B), else two.

@@ -46,12 +46,20 @@ struct FusedFB {
     int tile;
 };
 
+// Rows n >= n_split of a GEMM's output go to a second matrix y2 (row
+// n - n_split, row stride ldy2); n_split must be a multiple of 128.
+struct SplitOut {
+    int n_split;
+    __nv_bfloat16 *y2;
+    int64_t ldy2;
+};
+
 // tcgen05 cluster split-K kernel (kp_tc05.cu)
 bool tc05_supported(int M, int N, int K, const kp_cfg &c);
 bool tc05_fusable(int M, const kp_cfg &c);
 Scratch tc05_scratch(int M, int N, int K, const kp_cfg &c, int num_sms);
 cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStream_t s,
-                        const FusedFB *fb = nullptr);
+                        const FusedFB *fb = nullptr, const SplitOut *split = nullptr);
 int tc05_max_stages(int M);
 kp_cfg tc05_default(int M, int N, int K, int num_sms);
 

@@ -58,6 +58,11 @@ constexpr int kBarBytes = 512;
 struct Tc05Params {
     __nv_bfloat16 *y;
     int64_t ldy;
+    // Rows n >= n_split go to y2[m * ldy2 + (n - n_split)] (one launch over a
+    // packed weight writing two outputs); n_split >= N: y only. Multiple of 128.
+    int n_split;
+    __nv_bfloat16 *y2;
+    int64_t ldy2;
     int *err;
     int M, N, Mpad;
     int KB;            // K blocks in K
@@ -87,6 +92,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo) {
     return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
            (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(2) << 61);
+}
+
+__device__ __forceinline__ void store_y(const Tc05Params &p, int m, int n, __nv_bfloat16 v) {
+    if (n < p.n_split)
+        p.y[m * p.ldy + n] = v;
+    else
+        p.y2[m * p.ldy2 + (n - p.n_split)] = v;
 }
 
 // Byte offset of element (token m, feature k) of the fused F_B's B operand:
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float f = __uint_as_float(v[i]);
                     if (C == 1) {
                         const __nv_bfloat16 b = __float2bfloat16_rn(f);
-                        if (n < p.N) p.y[m * p.ldy + n] = b;
+                        if (n < p.N) store_y(p, m, n, b);
                         if (fused)
                             *reinterpret_cast<__nv_bfloat16 *>(gbase + p.off_bfa +
                                                               bfa_offset(m, row, p.Mpad)) = b;
@@ -317,15 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc.w += part[c].w;
                 }
             const int nb = tile * kTileN + rr;
-            __nv_bfloat16 *yr = p.y + m * p.ldy;
             const __nv_bfloat16 b0 = __float2bfloat16_rn(acc.x);
             const __nv_bfloat16 b1 = __float2bfloat16_rn(acc.y);
             const __nv_bfloat16 b2 = __float2bfloat16_rn(acc.z);
             const __nv_bfloat16 b3 = __float2bfloat16_rn(acc.w);
-            if (nb + 0 < p.N) yr[nb + 0] = b0;
-            if (nb + 1 < p.N) yr[nb + 1] = b1;
-            if (nb + 2 < p.N) yr[nb + 2] = b2;
-            if (nb + 3 < p.N) yr[nb + 3] = b3;
+            if (nb + 0 < p.N) store_y(p, m, nb + 0, b0);
+            if (nb + 1 < p.N) store_y(p, m, nb + 1, b1);
+            if (nb + 2 < p.N) store_y(p, m, nb + 2, b2);
+            if (nb + 3 < p.N) store_y(p, m, nb + 3, b3);
             if (fused) {
                 // this rank's features rr..rr+3 of the F_B operand (8 bytes)
                 __nv_bfloat162 lo, hi;
@@ -589,7 +600,7 @@ bool tc05_fusable(int M, const kp_cfg &c) {
 }
 
 cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStream_t stream,
-                        const FusedFB *fb) {
+                        const FusedFB *fb, const SplitOut *split) {
     (void)num_sms;
     if (!tc05_supported(a.M, a.N, a.K, c)) return cudaErrorInvalidValue;
     if (fb && !tc05_fusable(a.M, c)) return cudaErrorInvalidValue;
@@ -599,6 +610,15 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     Tc05Params p;
     p.y = a.y;
     p.ldy = a.ldy;
+    p.n_split = a.N;
+    p.y2 = nullptr;
+    p.ldy2 = 0;
+    if (split) {
+        if (split->n_split % kTileN) return cudaErrorInvalidValue;
+        p.n_split = split->n_split;
+        p.y2 = split->y2;
+        p.ldy2 = split->ldy2;
+    }
     p.err = a.err;
     p.M = a.M;
     p.N = a.N;

@@ -193,9 +193,18 @@ KP_API int skinny_gemm_noalloc(const void *x, const void *W, void *y, int M, int
  * Returns KP_OK, KP_EINVAL, KP_ESHAPE, KP_ENODEV or KP_ECUDA. */
 KP_API int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_plan **out);
 
-/* Overlap mode: -1 = per-M flag from the table (default), 0 = always
- * sequential on main_stream, 1 = always overlapped (when aux and events are
- * given). Returns KP_OK, KP_ENOPLAN, KP_EINVAL. */
+/* Execution mode: -1 = per-M choice from the table (default);
+ * 0 = sequential: Q/K/V/G, F_A/beta, F_B in order on main_stream;
+ * 1 = overlapped: F_A/beta -> F_B on aux_stream concurrently with Q/K/V/G on
+ *     main_stream (needs aux_stream and events, else runs as 0);
+ * 2 = single launch: one tcgen05 launch over the packed weight computes
+ *     Q/K/V/G and F_A/beta side by side, and the F_A tile's CTAs compute F_B
+ *     (needs a tcgen05 Q/K/V/G configuration, N_qkvg % 128 == 0, M <= 256 and
+ *     room for the F_B operands, else runs as 1). out_qkvg is bit-identical in
+ *     all modes; out_fab and out_fb are bit-identical between modes 0 and 1,
+ *     and equal to them in mode 2 when the F_A/beta configuration has the same
+ *     split-K factor as the Q/K/V/G one (otherwise within the tolerance).
+ * Returns KP_OK, KP_ENOPLAN, KP_EINVAL. */
 KP_API int kda_proj_set_overlap(kda_plan *plan, int mode);
 
 /* Branch ids for kda_proj_get_config / kda_proj_set_config. */
@@ -207,7 +216,7 @@ enum kp_branch { KP_BRANCH_QKVG = 0, KP_BRANCH_FAB = 1, KP_BRANCH_FB = 2 };
 KP_API int kda_proj_get_config(const kda_plan *plan, int branch, int M, kp_cfg *out);
 KP_API int kda_proj_set_config(kda_plan *plan, int branch, int M, const kp_cfg *cfg);
 
-/* Whether the plan overlaps at this M (1) or runs sequentially (0). */
+/* The mode the plan uses at this M (0, 1 or 2; see kda_proj_set_overlap). */
 KP_API int kda_proj_overlap_at(const kda_plan *plan, int M);
 
 /* ---------------------------------------------------------------------------
@@ -219,12 +228,12 @@ KP_API int kda_proj_overlap_at(const kda_plan *plan, int M);
  *   out_fab   device [M, N_fab] bf16 (written; columns 0..127 are F_A, the
  *             rest beta; F_B reads F_A from here)
  *   out_fb    device [M, N_fb] bf16 (written)
- *   main_stream, aux_stream, events[2]: caller-owned. When the plan overlaps
- *   at this M and aux_stream and events are all non-NULL, the F_A/beta -> F_B
- *   branch runs on aux_stream, forked from and joined back into main_stream
- *   with events[0] / events[1]; otherwise all three kernels run in order on
- *   main_stream. Either way, on return main_stream is ordered after all
- *   outputs. The sequence allocates nothing and never synchronises, so it can
+ *   main_stream, aux_stream, events[2]: caller-owned. The plan's mode at this
+ *   M (kda_proj_set_overlap) decides the schedule: overlapped (F_A/beta -> F_B
+ *   on aux_stream, forked from and joined back into main_stream with
+ *   events[0] / events[1]; needs aux_stream and both events), sequential (all
+ *   in order on main_stream) or a single launch on main_stream. Either way, on
+ *   return main_stream is ordered after all outputs. The sequence allocates nothing and never synchronises, so it can
  *   be captured into a CUDA graph (capture main_stream; aux joins through
  *   events[0]).
  * Returns KP_OK, KP_ENOPLAN, KP_EINVAL, KP_EALIGN, KP_ETOOBIG, KP_ECUDA. */

@@ -366,6 +366,73 @@ def test_kda_fused_fb_graph_replay(plan):
         plan.set_overlap(-1)
 
 
+# ---- the whole projection as one launch (mode 2) -------------------------------------------
+
+def _run_mode(plan, x, wp, wfb, mode, aux, evs):
+    M = x.shape[0]
+    outs = (poisoned((M, 4096)), poisoned((M, 136)), poisoned((M, 1024)))
+    plan.set_overlap(mode)
+    plan.run(x, wp, wfb, *outs, aux_stream=aux, events=evs)
+    torch.cuda.synchronize()
+    return [o.clone() for o in outs]
+
+
+@pytest.mark.parametrize("M", [1, 3, 16, 64, 128])
+@pytest.mark.parametrize("C,nkb", [(4, 2), (8, 2), (16, 4)])
+def test_kda_single_launch(plan, M, C, nkb):
+    cq = KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=0)
+    cf = KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=0)
+    saved = [plan.get_config(b, M) for b in range(3)]
+    try:
+        try:
+            plan.set_config(binding.BRANCH_QKVG, M, cq)
+            plan.set_config(binding.BRANCH_FAB, M, cf)
+        except binding.KdaProjError as e:
+            pytest.skip(str(e))
+        x, wp, wfb = kda_inputs(M, layer=6, seed=8)
+        x, wp, wfb = x.cuda(), wp.cuda(), wfb.cuda()
+        aux = torch.cuda.Stream()
+        evs = binding.make_events()
+        one = _run_mode(plan, x, wp, wfb, 2, aux, evs)
+        check_kda(one, x.cpu(), wp.cpu(), wfb.cpu(), 4096, 136, f"single launch C={C} M={M}")
+        seq = _run_mode(plan, x, wp, wfb, 0, aux, evs)
+        # same split-K factor for both branches: identical to the sequential path
+        assert torch.equal(one[0], seq[0]) and torch.equal(one[1], seq[1])
+        # F_B: same MMA sequence as the tcgen05 kernel with one CTA per tile
+        ref_fb = binding.skinny_gemm(one[1][:, :128].contiguous(), wfb,
+                                     cfg=KpCfg.make("tc05", split_k=1, k_unroll=2))
+        torch.cuda.synchronize()
+        assert torch.equal(ref_fb, one[2])
+        # captured and replayed
+        outs = (poisoned((M, 4096)), poisoned((M, 136)), poisoned((M, 1024)))
+        plan.set_overlap(2)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            plan.run(x, wp, wfb, *outs, aux_stream=aux, events=evs)
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(one, outs):
+            assert torch.equal(a, b)
+    finally:
+        for b, c in enumerate(saved):
+            plan.set_config(b, M, c)
+        plan.set_overlap(-1)
+
+
+def test_single_launch_falls_back_for_a_cuda_core_config(plan):
+    M = 2
+    saved = plan.get_config(binding.BRANCH_QKVG, M)
+    try:
+        plan.set_config(binding.BRANCH_QKVG, M, KpCfg.make("cc", split_k=1, rows=2, k_unroll=4))
+        x, wp, wfb = kda_inputs(M, layer=7, seed=9)
+        outs = _run_mode(plan, x.cuda(), wp.cuda(), wfb.cuda(), 2, torch.cuda.Stream(),
+                         binding.make_events())
+        check_kda(outs, x, wp, wfb, 4096, 136, "mode 2 fallback")
+    finally:
+        plan.set_config(binding.BRANCH_QKVG, M, saved)
+        plan.set_overlap(-1)
+
+
 # ---- boundary errors on a live device -------------------------------------------------------
 
 def test_errors_on_device(plan):
