@@ -71,6 +71,13 @@ struct Tc05Params {
     int x3d;           // 1: x of a full stage is one 3-D box (K % 64 == 0)
     int producers;     // warps issuing TMA copies (1..5)
     int stages;
+    // Push reduction (C > 1, tiles without the fused F_B): CTA 0 streams K
+    // blocks [0, r0_blocks), the others split the rest evenly; CTA 0 then
+    // receives their partial tiles and reduces.
+    int push;
+    int r0_blocks;
+    int n_tiles;       // feature tiles in the grid
+    int tile_rot;      // cluster i of the launch order computes tile (i + tile_rot) % n_tiles
     // Fused F_B: the CTAs of tile `fb_tile` (whose 128 rows are F_A) also
     // compute yfb = bf16(bf16(F_A) * W_fb^T); -1 = no fusion.
     int fb_tile;
@@ -131,18 +138,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *fbw = accf + 1;      // fused F_B: W_fb tile landed
     uint64_t *fbacc = fbw + 1;     // fused F_B: accumulator ready
     uint64_t *fbempty = fbacc + 1; // fused F_B: accumulator drained
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fbempty + 1);
+    uint64_t *recv = fbempty + 1;  // push reduction (CTA 0): peers' partial tiles landed
+    uint64_t *go = recv + 1;       // push reduction (CTA r > 0): CTA 0 can receive
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(go + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int C = p.C;
     const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int tile = blockIdx.x / C;
-    const int kb0 = static_cast<int>((static_cast<long long>(p.KB) * rank) / C);
-    const int kb1 = static_cast<int>((static_cast<long long>(p.KB) * (rank + 1)) / C);
-    const int n_st = (kb1 - kb0 + p.nkb - 1) / p.nkb;  // stages of work for this CTA
+    // The fused F_B tile (if any) is dispatched first: its cluster has the
+    // longest epilogue.
+    const int tile = (static_cast<int>(blockIdx.x) / C + p.tile_rot) % p.n_tiles;
     const bool fused = (p.fb_tile >= 0 && tile == p.fb_tile);
+    const bool push = p.push && C > 1 && !fused;   // uniform over the cluster
+    int kb0, kb1;
+    if (!push) {
+        kb0 = static_cast<int>((static_cast<long long>(p.KB) * rank) / C);
+        kb1 = static_cast<int>((static_cast<long long>(p.KB) * (rank + 1)) / C);
+    } else if (rank == 0) {
+        kb0 = 0;
+        kb1 = p.r0_blocks;
+    } else {
+        const long long rest = p.KB - p.r0_blocks;
+        kb0 = p.r0_blocks + static_cast<int>((rest * (rank - 1)) / (C - 1));
+        kb1 = p.r0_blocks + static_cast<int>((rest * rank) / (C - 1));
+    }
+    const int n_st = (kb1 - kb0 + p.nkb - 1) / p.nkb;  // stages of work for this CTA
     // fused F_B tiles of this CTA: rank, rank + C, ...
     const int my_fb = fused && rank < p.fb_tiles ? (p.fb_tiles - rank + C - 1) / C : 0;
 
@@ -155,6 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(fbw), 1);
         mbar_init(smem_u32(fbacc), 1);
         mbar_init(smem_u32(fbempty), 4);
+        mbar_init(smem_u32(recv), 1);
+        mbar_init(smem_u32(go), 1);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmw);
@@ -170,6 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Peers signal each other's barriers only after the matching wait.
+    if (push) cluster_arrive_relaxed();
     pdl_trigger();
 
     // producer index of this warp's lane 0 (-1: not a producer)
@@ -279,6 +305,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         float *red = reinterpret_cast<float *>(gbase);  // [Mpad][128] fp32, reuses stage memory
+        if (push) {
+            // Slot c - 1 (c = 1..C-1) of CTA 0's stage memory holds CTA c's
+            // partial tile as [M][128] fp32; CTA 0 adds them to its own in
+            // rank order, so the sum order is fixed.
+            const uint32_t slot_bytes = static_cast<uint32_t>(p.M) * kTileN * 4;
+            __syncwarp();
+            cluster_wait();
+            if (rank == 0) {
+                if (warp == 2 && lane == 0) {
+                    mbar_expect_tx(smem_u32(recv), static_cast<uint32_t>(C - 1) * slot_bytes);
+                    for (int c = 1; c < C; ++c)
+                        mbar_arrive_remote(mapa_shared(smem_u32(go), static_cast<uint32_t>(c)));
+                }
+                mbar_wait_bounded<true>(smem_u32(recv), 0, abort_flag, p.err, DEV_TIMEOUT_PEER);
+                for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = c0 + i;
+                        if (m < p.M) {
+                            float acc = __uint_as_float(v[i]);
+                            const float *src = red + m * kTileN + row;
+                            for (int c = 1; c < C; ++c)
+                                acc += src[static_cast<size_t>(c - 1) * p.M * kTileN];
+                            if (n < p.N) store_y(p, m, n, __float2bfloat16_rn(acc));
+                        }
+                    }
+                }
+            } else if (mbar_wait_bounded<true>(smem_u32(go), 0, abort_flag, p.err, DEV_TIMEOUT_PEER)) {
+                const uint32_t rbar = mapa_shared(smem_u32(recv), 0);
+                const uint32_t dst = mapa_shared(
+                    base + static_cast<uint32_t>(rank - 1) * slot_bytes + static_cast<uint32_t>(row) * 4, 0);
+                for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = c0 + i;
+                        if (m < p.M)
+                            st_async_f32(dst + static_cast<uint32_t>(m) * kTileN * 4,
+                                         __uint_as_float(v[i]), rbar);
+                    }
+                }
+            }
+        } else
         for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(taddr + c0, v);
@@ -303,7 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
     }
 
-    if (C > 1) {
+    if (push && warp < 2) {
+        __syncwarp();
+        cluster_wait();   // pairs with the early arrive
+    }
+
+    if (C > 1 && !push) {
         // All partial tiles of the cluster are in shared memory after this.
         __syncwarp();
         cluster_sync_all();
@@ -570,7 +649,11 @@ bool tc05_supported(int M, int N, int K, const kp_cfg &c) {
     const int st = c.stages ? c.stages : ms;
     if (st < 1 || st > ms) return false;
     // the cluster reduction reuses the stage memory for an Mpad x 128 fp32 tile
-    if (C > 1 && static_cast<size_t>(Mpad) * kTileN * 4 > static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb))
+    const size_t pipe = static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb);
+    if (C > 1 && static_cast<size_t>(Mpad) * kTileN * 4 > pipe) return false;
+    // push reduction: CTA 0 holds C - 1 partial tiles of M x 128 fp32
+    if (C > 1 && (c.flags & KP_FLAG_PUSH_REDUCE) &&
+        static_cast<size_t>(C - 1) * M * kTileN * 4 > pipe)
         return false;
     return true;
 }
@@ -628,6 +711,14 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.nkb = nkb;
     p.producers = producers_of(c);
     p.stages = stages;
+    p.push = (p.C > 1 && (c.flags & KP_FLAG_PUSH_REDUCE)) ? 1 : 0;
+    // CTA 0 takes about 3/4 of an even share, so it is usually ready to
+    // receive before the others finish; every other CTA keeps >= 1 block.
+    p.r0_blocks = (p.KB * 3) / (4 * p.C);
+    if (p.r0_blocks < 1) p.r0_blocks = 1;
+    if (p.r0_blocks > p.KB - (p.C - 1)) p.r0_blocks = p.KB - (p.C - 1);
+    p.n_tiles = (a.N + kTileN - 1) / kTileN;
+    p.tile_rot = 0;
     // kind::f16 instruction descriptor: D fp32 (bit 4), A and B bf16 (bits
     // 7, 10), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
     p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(Mpad >> 3) << 17) |
@@ -647,6 +738,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
         uint32_t end;
         fb_layout(Mpad, &p.off_bfa, &p.off_wfb, &end);
         p.fb_tile = fb->tile;
+        p.tile_rot = fb->tile;
         p.N_fb = fb->N;
         p.fb_tiles = (fb->N + kTileN - 1) / kTileN;
         p.yfb = fb->y;
