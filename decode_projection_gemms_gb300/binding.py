@@ -28,7 +28,6 @@ KIND_AUTO, KIND_CC, KIND_TC05, KIND_SMALLK = 0, 1, 2, 3
 KIND_NAMES = {0: "auto", 1: "cc", 2: "tc05", 3: "smallk"}
 FLAG_PDL = 1
 FLAG_FUSE_FB = 2
-FLAG_PUSH_REDUCE = 4
 BRANCH_QKVG, BRANCH_FAB, BRANCH_FB = 0, 1, 2
 
 # exported symbols (must match include/kdaproj.h)

@@ -76,8 +76,7 @@ enum DevErr {
     DEV_TIMEOUT_FULL = 1,     // MMA warp waited too long for a TMA stage
     DEV_TIMEOUT_EMPTY = 2,    // producer waited too long for a free stage
     DEV_TIMEOUT_ACC_FULL = 3, // epilogue waited too long for an accumulator
-    DEV_TIMEOUT_ACC_EMPTY = 4, // MMA warp waited too long for a free accumulator
-    DEV_TIMEOUT_PEER = 5       // a cluster peer's signal or partial tile never came
+    DEV_TIMEOUT_ACC_EMPTY = 4 // MMA warp waited too long for a free accumulator
 };
 
 }  // namespace kp
@@ -148,19 +147,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Same, with acquire at cluster scope: for barriers that other CTAs' st.async
-// writes or remote arrivals complete.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -172,17 +158,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // raises the CTA's abort flag and returns false. The caller then proceeds as
 // if the phase had completed: every address it touches stays in bounds, so a
 // broken pipeline yields wrong numbers and an error code, never a hang.
-template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort_flag, int *err,
                                                   int code) {
-    auto ready = [&] {
-        return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-    };
-    if (ready()) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (ready()) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > 1000000000ull) {
             *abort_flag = 1;
@@ -276,45 +258,6 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Split cluster barrier: arrive early (no ordering beyond the mbarrier-init
-// fence that precedes it), wait later with acquire semantics.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster;
-// `bar` is a shared::cluster address from mapa_shared.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
-                 : "memory");
-}
-// Asynchronous store into another CTA's shared memory that counts its bytes on
-// that CTA's mbarrier (complete_tx). Both addresses are shared::cluster ones.
-__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
-                     addr),
-                 "r"(__float_as_uint(v)), "r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
-            addr),
-        "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(bar)
-        : "memory");
-}
-__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float a, float b, float c, float d,
-                                               uint32_t bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
-        "[%5];" ::"r"(addr),
-        "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(__float_as_uint(c)),
-        "r"(__float_as_uint(d)), "r"(bar)
-        : "memory");
-}
-
 // Address of the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     uint32_t r;

@@ -71,11 +71,6 @@ struct Tc05Params {
     int x3d;           // 1: x of a full stage is one 3-D box (K % 64 == 0)
     int producers;     // warps issuing TMA copies (1..5)
     int stages;
-    // Push reduction (C > 1, tiles without the fused F_B): CTA 0 streams K
-    // blocks [0, r0_blocks), the others split the rest evenly; CTA 0 then
-    // receives their partial tiles and reduces.
-    int push;
-    int r0_blocks;
     int n_tiles;       // feature tiles in the grid
     int tile_rot;      // cluster i of the launch order computes tile (i + tile_rot) % n_tiles
     // Fused F_B: the CTAs of tile `fb_tile` (whose 128 rows are F_A) also
@@ -138,9 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *fbw = accf + 1;      // fused F_B: W_fb tile landed
     uint64_t *fbacc = fbw + 1;     // fused F_B: accumulator ready
     uint64_t *fbempty = fbacc + 1; // fused F_B: accumulator drained
-    uint64_t *recv = fbempty + 1;  // push reduction (CTA 0): peers' partial tiles landed
-    uint64_t *go = recv + 1;       // push reduction (CTA r > 0): CTA 0 can receive
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(go + 1);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fbempty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -151,23 +144,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // longest epilogue.
     const int tile = (static_cast<int>(blockIdx.x) / C + p.tile_rot) % p.n_tiles;
     const bool fused = (p.fb_tile >= 0 && tile == p.fb_tile);
-    const bool push = p.push && C > 1 && !fused;   // uniform over the cluster
-    int kb0, kb1;
-    if (!push) {
-        kb0 = static_cast<int>((static_cast<long long>(p.KB) * rank) / C);
-        kb1 = static_cast<int>((static_cast<long long>(p.KB) * (rank + 1)) / C);
-    } else if (rank == 0) {
-        kb0 = 0;
-        kb1 = p.r0_blocks;
-    } else {
-        const long long rest = p.KB - p.r0_blocks;
-        kb0 = p.r0_blocks + static_cast<int>((rest * (rank - 1)) / (C - 1));
-        kb1 = p.r0_blocks + static_cast<int>((rest * rank) / (C - 1));
-    }
+    const int kb0 = static_cast<int>((static_cast<long long>(p.KB) * rank) / C);
+    const int kb1 = static_cast<int>((static_cast<long long>(p.KB) * (rank + 1)) / C);
     const int n_st = (kb1 - kb0 + p.nkb - 1) / p.nkb;  // stages of work for this CTA
     // fused F_B tiles of this CTA: rank, rank + C, ...
     const int my_fb = fused && rank < p.fb_tiles ? (p.fb_tiles - rank + C - 1) / C : 0;
 
+    // producer index of this warp's lane 0 (-1: not a producer)
+    const int pidx = (warp == 0) ? 0 : (warp >= 2 && warp - 1 < p.producers) ? warp - 1 : -1;
+    const int P = p.producers;
+    const uint32_t xblk = static_cast<uint32_t>(p.Mpad) * kBlockK * 2;
+    const int row0 = tile * kTileN;
+    const int pre = n_st < S ? n_st : S;
+    // W boxes of stage s of this CTA's range, producer pidx's share; producer
+    // 0 also accounts for the stage's x bytes.
+    auto issue_w = [&](int s, int stage, uint64_t pol_w) {
+        const int k0 = kb0 + s * p.nkb;
+        const int kbs = min(p.nkb, kb1 - k0);
+        const uint32_t st = base + stage * p.stage_bytes;
+        const uint32_t bar = smem_u32(full + stage);
+        int mine = 0;
+        for (int j = pidx; j < kbs; j += P) ++mine;
+        uint32_t bytes = static_cast<uint32_t>(mine) * kWBlockBytes;
+        if (pidx == 0) bytes += static_cast<uint32_t>(kbs) * xblk;
+        mbar_expect_tx(bar, bytes);   // every producer arrives once per stage
+        for (int j = pidx; j < kbs; j += P)
+            tma_load_2d(st + j * kWBlockBytes, &tmw, bar, (k0 + j) * kBlockK, row0, pol_w);
+    };
+    pdl_trigger();
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(full + s), static_cast<uint32_t>(p.producers));
@@ -177,11 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(fbw), 1);
         mbar_init(smem_u32(fbacc), 1);
         mbar_init(smem_u32(fbempty), 4);
-        mbar_init(smem_u32(recv), 1);
-        mbar_init(smem_u32(go), 1);
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmw);
+        // the weight stream starts before the TMEM allocation and the block barrier
+        for (int s = 0; s < pre; ++s) issue_w(s, s, policy_evict_first());
         tma_prefetch_desc(&tmx);
         if (p.x3d) tma_prefetch_desc(&tmx3);
         if (fused) tma_prefetch_desc(&tmfb);
@@ -194,35 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // Peers signal each other's barriers only after the matching wait.
-    if (push) cluster_arrive_relaxed();
-    pdl_trigger();
 
-    // producer index of this warp's lane 0 (-1: not a producer)
-    const int pidx = (warp == 0) ? 0 : (warp >= 2 && warp - 1 < p.producers) ? warp - 1 : -1;
     if (pidx >= 0 && lane == 0) {
         // ---------------- TMA producers ----------------
-        const int P = p.producers;
         const uint64_t pol_w = policy_evict_first();
         const uint64_t pol_x = policy_evict_last();
-        const uint32_t xblk = static_cast<uint32_t>(p.Mpad) * kBlockK * 2;
-        const int row0 = tile * kTileN;
         // A full stage's x is one 3-D box; a short last stage uses one 2-D box
         // per K block (so nothing past this CTA's range is read).
         auto x_full = [&](int kbs) { return p.x3d && kbs == p.nkb; };
-        auto issue_w = [&](int s, int stage) {
-            const int k0 = kb0 + s * p.nkb;
-            const int kbs = min(p.nkb, kb1 - k0);
-            const uint32_t st = base + stage * p.stage_bytes;
-            const uint32_t bar = smem_u32(full + stage);
-            int mine = 0;
-            for (int j = pidx; j < kbs; j += P) ++mine;
-            uint32_t bytes = static_cast<uint32_t>(mine) * kWBlockBytes;
-            if (pidx == 0) bytes += static_cast<uint32_t>(kbs) * xblk;
-            mbar_expect_tx(bar, bytes);   // every producer arrives once per stage
-            for (int j = pidx; j < kbs; j += P)
-                tma_load_2d(st + j * kWBlockBytes, &tmw, bar, (k0 + j) * kBlockK, row0, pol_w);
-        };
         auto issue_x = [&](int s, int stage) {
             const int k0 = kb0 + s * p.nkb;
             const int kbs = min(p.nkb, kb1 - k0);
@@ -235,10 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(st + j * xblk, &tmx, bar, (k0 + j) * kBlockK, 0, pol_x);
             }
         };
-        const int pre = n_st < S ? n_st : S;
         // Weights never depend on the previous kernel: the first stages' W
-        // tiles go out before waiting for it; x (producer 0) follows after.
-        for (int s = 0; s < pre; ++s) issue_w(s, s);
+        // tiles go out before waiting for it (producer 0's right after the
+        // barriers are initialised); x (producer 0) follows after the wait.
+        if (pidx != 0)
+            for (int s = 0; s < pre; ++s) issue_w(s, s, pol_w);
         if (pidx == 0) {
             pdl_wait();
             for (int s = 0; s < pre; ++s) issue_x(s, s);
@@ -247,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int stage = s % S;
             mbar_wait_bounded(smem_u32(empty + stage), static_cast<uint32_t>(((s / S) - 1) & 1),
                               abort_flag, p.err, DEV_TIMEOUT_EMPTY);
-            issue_w(s, stage);
+            issue_w(s, stage, pol_w);
             if (pidx == 0) issue_x(s, stage);
         }
         if (*abort_flag) {
@@ -305,54 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         float *red = reinterpret_cast<float *>(gbase);  // [Mpad][128] fp32, reuses stage memory
-        if (push) {
-            // Slot c - 1 (c = 1..C-1) of CTA 0's stage memory holds CTA c's
-            // partial tile as [M][128] fp32; CTA 0 adds them to its own in
-            // rank order, so the sum order is fixed.
-            const uint32_t slot_bytes = static_cast<uint32_t>(p.M) * kTileN * 4;
-            __syncwarp();
-            cluster_wait();
-            if (rank == 0) {
-                if (warp == 2 && lane == 0) {
-                    mbar_expect_tx(smem_u32(recv), static_cast<uint32_t>(C - 1) * slot_bytes);
-                    for (int c = 1; c < C; ++c)
-                        mbar_arrive_remote(mapa_shared(smem_u32(go), static_cast<uint32_t>(c)));
-                }
-                mbar_wait_bounded<true>(smem_u32(recv), 0, abort_flag, p.err, DEV_TIMEOUT_PEER);
-                for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(taddr + c0, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = c0 + i;
-                        if (m < p.M) {
-                            float acc = __uint_as_float(v[i]);
-                            const float *src = red + m * kTileN + row;
-                            for (int c = 1; c < C; ++c)
-                                acc += src[static_cast<size_t>(c - 1) * p.M * kTileN];
-                            if (n < p.N) store_y(p, m, n, __float2bfloat16_rn(acc));
-                        }
-                    }
-                }
-            } else if (mbar_wait_bounded<true>(smem_u32(go), 0, abort_flag, p.err, DEV_TIMEOUT_PEER)) {
-                const uint32_t rbar = mapa_shared(smem_u32(recv), 0);
-                const uint32_t dst = mapa_shared(
-                    base + static_cast<uint32_t>(rank - 1) * slot_bytes + static_cast<uint32_t>(row) * 4, 0);
-                for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(taddr + c0, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = c0 + i;
-                        if (m < p.M)
-                            st_async_f32(dst + static_cast<uint32_t>(m) * kTileN * 4,
-                                         __uint_as_float(v[i]), rbar);
-                    }
-                }
-            }
-        } else
         for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
             uint32_t v[16];
             tmem_ld16(taddr + c0, v);
@@ -377,12 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
     }
 
-    if (push && warp < 2) {
-        __syncwarp();
-        cluster_wait();   // pairs with the early arrive
-    }
-
-    if (C > 1 && !push) {
+    if (C > 1) {
         // All partial tiles of the cluster are in shared memory after this.
         __syncwarp();
         cluster_sync_all();
@@ -649,11 +579,7 @@ bool tc05_supported(int M, int N, int K, const kp_cfg &c) {
     const int st = c.stages ? c.stages : ms;
     if (st < 1 || st > ms) return false;
     // the cluster reduction reuses the stage memory for an Mpad x 128 fp32 tile
-    const size_t pipe = static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb);
-    if (C > 1 && static_cast<size_t>(Mpad) * kTileN * 4 > pipe) return false;
-    // push reduction: CTA 0 holds C - 1 partial tiles of M x 128 fp32
-    if (C > 1 && (c.flags & KP_FLAG_PUSH_REDUCE) &&
-        static_cast<size_t>(C - 1) * M * kTileN * 4 > pipe)
+    if (C > 1 && static_cast<size_t>(Mpad) * kTileN * 4 > static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb))
         return false;
     return true;
 }
@@ -711,12 +637,6 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.nkb = nkb;
     p.producers = producers_of(c);
     p.stages = stages;
-    p.push = (p.C > 1 && (c.flags & KP_FLAG_PUSH_REDUCE)) ? 1 : 0;
-    // CTA 0 takes about 3/4 of an even share, so it is usually ready to
-    // receive before the others finish; every other CTA keeps >= 1 block.
-    p.r0_blocks = (p.KB * 3) / (4 * p.C);
-    if (p.r0_blocks < 1) p.r0_blocks = 1;
-    if (p.r0_blocks > p.KB - (p.C - 1)) p.r0_blocks = p.KB - (p.C - 1);
     p.n_tiles = (a.N + kTileN - 1) / kTileN;
     p.tile_rot = 0;
     // kind::f16 instruction descriptor: D fp32 (bit 4), A and B bf16 (bits

@@ -91,16 +91,9 @@ enum kp_flags {
                            kernel may start (and stream its weights) while the
                            previous kernel on the stream finishes; it waits for
                            that kernel before touching x, y or scratch */
-    KP_FLAG_FUSE_FB = 2, /* F_A/beta branch of kda_proj_run only (TC05 kind,
-                            M <= 256): the F_A/beta launch also computes F_B
-                            from its bf16 F_A tile, so the F_B launch is skipped */
-    KP_FLAG_PUSH_REDUCE = 4 /* TC05 with split_k > 1: CTA 0 of each cluster
-                               takes a smaller share of K and, once its own
-                               loop is done, receives the other CTAs' fp32
-                               partial tiles in its shared memory and sums
-                               them in rank order; the others leave as soon as
-                               their partial is sent. Needs (split_k - 1) x
-                               128 x M x 4 bytes of pipeline memory */
+    KP_FLAG_FUSE_FB = 2 /* F_A/beta branch of kda_proj_run only (TC05 kind,
+                           M <= 256): the F_A/beta launch also computes F_B
+                           from its bf16 F_A tile, so the F_B launch is skipped */
 };
 
 /* One kernel configuration. Fields a kind does not use are ignored. */
@@ -210,9 +203,7 @@ KP_API int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_
  *     room for the F_B operands, else runs as 1). out_qkvg is bit-identical in
  *     all modes; out_fab and out_fb are bit-identical between modes 0 and 1,
  *     and equal to them in mode 2 when the F_A/beta configuration has the same
- *     split-K factor and KP_FLAG_PUSH_REDUCE setting as the Q/K/V/G one and,
- *     if that flag is set, also KP_FLAG_FUSE_FB (otherwise within the
- *     tolerance).
+ *     split-K factor as the Q/K/V/G one (otherwise within the tolerance).
  * Returns KP_OK, KP_ENOPLAN, KP_EINVAL. */
 KP_API int kda_proj_set_overlap(kda_plan *plan, int mode);
 

@@ -136,16 +136,6 @@ def test_scratch_sizes(lib):
                    binding.KpCfg.make("tc05", producers=6)):
         with pytest.raises(binding.KdaProjError):
             binding.scratch_bytes(20, 4096, 7168, bad_tc, 152)
-    # push reduction: CTA 0 receives split_k - 1 partial tiles of M x 128 fp32
-    # in its pipeline memory (no scratch either)
-    push = binding.KpCfg.make("tc05", split_k=8, k_unroll=2, stages=3,
-                              flags=binding.FLAG_PDL | binding.FLAG_PUSH_REDUCE)
-    assert binding.scratch_bytes(16, 4096, 7168, push, 152) == 0
-    push16 = binding.KpCfg.make("tc05", split_k=16, k_unroll=2, stages=2,
-                                flags=binding.FLAG_PUSH_REDUCE)
-    with pytest.raises(binding.KdaProjError) as e:
-        binding.scratch_bytes(128, 4096, 7168, push16, 152)   # 15 x 64 KB > pipeline
-    assert e.value.code == binding.KP_ECONFIG
     bad = binding.KpCfg.make("cc", split_k=1, block=256, rows=8, k_unroll=1)
     with pytest.raises(binding.KdaProjError) as e:
         binding.scratch_bytes(16, 4096, 7168, bad, 152)     # 8 x 16 accumulators: not built

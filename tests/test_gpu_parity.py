@@ -119,32 +119,6 @@ def test_tc05_cluster_splits(C, nkb):
                    f"tc05 P={P}")
 
 
-@pytest.mark.parametrize("M", [1, 2, 5, 16, 33, 64, 128])
-@pytest.mark.parametrize("C,nkb", [(2, 2), (4, 1), (8, 2), (16, 1)])
-def test_tc05_push_reduce(M, C, nkb):
-    # CTA 0 of each cluster takes a smaller K share and sums the others'
-    # partial tiles in rank order; N = 1000 leaves a ragged last tile
-    x, W = gemm_case(M, 1000, 7168, seed=400 + M + C)
-    cfg = KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=0,
-                     flags=binding.FLAG_PDL | binding.FLAG_PUSH_REDUCE)
-    try:
-        binding.scratch_bytes(M, 1000, 7168, cfg, 152)
-    except binding.KdaProjError as e:
-        assert e.code == binding.KP_ECONFIG
-        pytest.skip("partial tiles do not fit in the pipeline memory")
-    y1, _ = check_gemm(x, W, cfg, "tc05 push")
-    y2, _ = check_gemm(x, W, cfg, "tc05 push, again")
-    assert torch.equal(y1, y2)
-
-
-def test_tc05_push_reduce_short_k():
-    # K = 1032: 17 K blocks, the last one ragged; CTA 0 keeps one block
-    for C in (2, 8, 16):
-        x, W = gemm_case(3, 136, 1032, seed=C)
-        check_gemm(x, W, KpCfg.make("tc05", split_k=C, k_unroll=1,
-                                    flags=binding.FLAG_PDL | binding.FLAG_PUSH_REDUCE), f"C={C}")
-
-
 def test_tc05_m_above_256_is_sliced():
     x, W = gemm_case(300, 264, 512, seed=8)
     check_gemm(x, W, KpCfg.make("tc05", split_k=4, k_unroll=1), "tc05")
@@ -405,14 +379,9 @@ def _run_mode(plan, x, wp, wfb, mode, aux, evs):
 
 @pytest.mark.parametrize("M", [1, 3, 16, 64, 128])
 @pytest.mark.parametrize("C,nkb", [(4, 2), (8, 2), (16, 4)])
-@pytest.mark.parametrize("push", [False, True])
-def test_kda_single_launch(plan, M, C, nkb, push):
-    fl = binding.FLAG_PDL | (binding.FLAG_PUSH_REDUCE if push else 0)
-    cq = KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=0, flags=fl)
-    # with push, the F_A tile of the single launch reduces by pulling (it
-    # computes F_B), like a fused F_A/beta launch does
-    cf = KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=0,
-                    flags=fl | (binding.FLAG_FUSE_FB if push else 0))
+def test_kda_single_launch(plan, M, C, nkb):
+    cq = KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=0)
+    cf = KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=0)
     saved = [plan.get_config(b, M) for b in range(3)]
     try:
         try:
