@@ -155,12 +155,15 @@ def sweep_shape(M, N, K, sms, device, kinds, verbose=False):
 
 class PlanBench:
     """Full KDA projection timing: a weight stack of packed [N_qkvg+N_fab, K]
-    + W_fb [N_fb, 128] layers (at least 4x L2), graph of `layers` calls."""
+    + W_fb [N_fb, 128] layers (at least 4x L2 and at least 48, the layer count
+    of the benchmark: each graph replay boundary breaks the chain of
+    programmatic dependent launches, so short graphs favour the wrong mode),
+    graph of `layers` calls."""
 
     def __init__(self, max_M, device, K=7168, Nq=4096, Nfab=136, Nfb=1024, seed=0):
         self.K, self.Nq, self.Nfab, self.Nfb = K, Nq, Nfab, Nfb
         per = ((Nq + Nfab) * K + Nfb * 128) * 2
-        self.layers = max(4, math.ceil(4 * L2_BYTES / per))
+        self.layers = max(48, math.ceil(4 * L2_BYTES / per))
         g = torch.Generator(device=device)
         g.manual_seed(seed)
         self.Wp = (torch.randn((self.layers, Nq + Nfab, K), generator=g, device=device) * 0.02).to(torch.bfloat16)
