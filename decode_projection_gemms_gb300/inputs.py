@@ -21,6 +21,9 @@ of a weight stack comes from a generator seeded with ``seed + 1 + l`` (the
 packed weight is drawn first, then ``W_fb``). Values are drawn in fp32 and
 rounded to bf16 with round-to-nearest-even by ``Tensor.to(torch.bfloat16)``.
 
+``dtype=torch.float16`` draws the same fp32 numbers and rounds them to fp16
+instead (the skinny GEMM's other input type).
+
 ``device="cpu"`` is the canonical stream that parity tests use. A CUDA device
 draws from torch's CUDA generator instead (different numbers, same
 distribution); the benchmark uses that for filler layers of large weight
@@ -46,8 +49,9 @@ def _gen(seed: int, device) -> torch.Generator:
     return g
 
 
-def gen_x(M: int, K: int, seed: int = 0, dist: str = "normal", device="cpu") -> torch.Tensor:
-    """Hidden states ``[M, K]`` bf16 drawn from ``dist`` with generator ``seed``."""
+def gen_x(M: int, K: int, seed: int = 0, dist: str = "normal", device="cpu",
+          dtype=torch.bfloat16) -> torch.Tensor:
+    """Hidden states ``[M, K]`` (bf16 or fp16) drawn from ``dist`` with generator ``seed``."""
     g = _gen(seed, device)
     if dist == "normal":
         v = torch.randn((M, K), generator=g, device=device, dtype=torch.float32)
@@ -55,18 +59,18 @@ def gen_x(M: int, K: int, seed: int = 0, dist: str = "normal", device="cpu") -> 
         v = torch.rand((M, K), generator=g, device=device, dtype=torch.float32) * 2.0 - 1.0
     else:
         raise ValueError(f"unknown dist {dist!r}")
-    return v.to(torch.bfloat16)
+    return v.to(dtype)
 
 
 def gen_w(N: int, K: int, seed: int, std: float = W_STD, device="cpu",
-          g: torch.Generator | None = None) -> torch.Tensor:
-    """Weight ``[N, K]`` bf16 ~N(0, std^2)."""
+          g: torch.Generator | None = None, dtype=torch.bfloat16) -> torch.Tensor:
+    """Weight ``[N, K]`` (bf16 or fp16) ~N(0, std^2)."""
     if g is None:
         g = _gen(seed, device)
     v = torch.randn((N, K), generator=g, device=device, dtype=torch.float32)
     if std != 1.0:
         v.mul_(std)
-    return v.to(torch.bfloat16)
+    return v.to(dtype)
 
 
 def gen_kda_layer(layer: int, seed: int = 0, K: int = K_HIDDEN, N_qkvg: int = N_QKVG,
@@ -87,6 +91,12 @@ def gen_gemm_layer(layer: int, N: int, K: int, seed: int = 0, device="cpu") -> t
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """Raw bf16 bit patterns of a CPU tensor as a contiguous ``uint16`` array."""
     assert t.dtype == torch.bfloat16
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    """Raw bit patterns of a bf16 or fp16 tensor as a contiguous ``uint16`` array."""
+    assert t.dtype in (torch.bfloat16, torch.float16)
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 

@@ -7,12 +7,15 @@ and it shares no code with the CUDA path: the arithmetic lives in
 passages it follows), and this module only compiles it with gcc, loads it with
 ctypes and moves numpy arrays in and out.
 
-Inputs are raw bf16 bit patterns (``numpy.uint16``); outputs are float64.
+Inputs are raw bf16 (or, for ``gemm_ex``, fp16) bit patterns
+(``numpy.uint16``); outputs are float64.
 
 Comparison criterion (the build's stated tolerance for bf16 outputs with fp32
 accumulation): ``|gpu - ref| <= 4 * ulp_bf16(|ref|) + 1e-3`` element-wise, with
 ``ulp_bf16(v) = 2^(floor(log2 v) - 7)`` for normal ``v`` (bf16 keeps 8
-significant bits) and ``2^-133`` below the normal range.
+significant bits) and ``2^-133`` below the normal range. fp16 outputs use the
+same rule with fp16's unit in the last place: ``2^(floor(log2 v) - 10)`` (11
+significant bits), ``2^-24`` below ``2^-14``.
 
 Parity pins: closed forms, one-hot selection, power-of-two scaling, row
 independence, exact rational brute force and hand-derived bf16 rounding cases
@@ -83,6 +86,12 @@ class Oracle:
         lib.kdo_widen_bf16.restype = None
         lib.kdo_gemm.argtypes = [u16p, i64, u16p, i64, f64p, i64, ci, ci, ci, ci]
         lib.kdo_gemm.restype = ci
+        lib.kdo_gemm_ex.argtypes = [u16p, i64, u16p, i64, u16p, i64, ci, f64p, i64, ci, ci, ci, ci]
+        lib.kdo_gemm_ex.restype = ci
+        lib.kdo_fp16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.kdo_fp16_to_f64.restype = ctypes.c_double
+        lib.kdo_widen_fp16.argtypes = [u16p, f64p, i64]
+        lib.kdo_widen_fp16.restype = None
         lib.kdo_kda_proj.argtypes = [u16p, u16p, u16p, f64p, f64p, u16p, f64p,
                                      ci, ci, ci, ci, ci, ci, ci]
         lib.kdo_kda_proj.restype = ci
@@ -106,6 +115,13 @@ class Oracle:
         self.lib.kdo_widen_bf16(_p(b, ctypes.c_uint16), _p(out, ctypes.c_double), b.size)
         return out
 
+    def fp16_to_f64(self, bits) -> np.ndarray:
+        """Exact widening of fp16 bit patterns to float64."""
+        b = _u16(bits)
+        out = np.empty(b.shape, dtype=np.float64)
+        self.lib.kdo_widen_fp16(_p(b, ctypes.c_uint16), _p(out, ctypes.c_double), b.size)
+        return out
+
     def f64_to_bf16(self, v) -> np.ndarray:
         """float64 -> bf16 bit patterns, round to nearest, ties to even."""
         a = np.ascontiguousarray(v, dtype=np.float64)
@@ -126,6 +142,30 @@ class Oracle:
                                _p(y, ctypes.c_double), N, M, N, K, int(nthreads))
         if rc:
             raise ValueError("kdo_gemm rejected its arguments")
+        return y
+
+    def gemm_ex(self, x_bits, w_bits, res_bits=None, dtype: str = "bf16",
+                nthreads: int = 1) -> np.ndarray:
+        """``y[m, n] = sum_k x[m, k] * W[n, k] + res[m, n]`` in double, inputs of
+        type ``dtype`` ("bf16" or "fp16"); ``res`` ``[M, N]`` or None."""
+        x = _u16(x_bits)
+        w = _u16(w_bits)
+        if x.ndim != 2 or w.ndim != 2 or x.shape[1] != w.shape[1]:
+            raise ValueError(f"shape mismatch {x.shape} vs {w.shape}")
+        M, K = x.shape
+        N = w.shape[0]
+        code = {"bf16": 0, "fp16": 1}[dtype]
+        r = None
+        if res_bits is not None:
+            r = _u16(res_bits)
+            if r.shape != (M, N):
+                raise ValueError(f"residual shape {r.shape} != {(M, N)}")
+        y = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.kdo_gemm_ex(_p(x, ctypes.c_uint16), K, _p(w, ctypes.c_uint16), K,
+                                  _p(r, ctypes.c_uint16) if r is not None else None, N, code,
+                                  _p(y, ctypes.c_double), N, M, N, K, int(nthreads))
+        if rc:
+            raise ValueError("kdo_gemm_ex rejected its arguments")
         return y
 
     def kda_proj(self, x_bits, wp_bits, wfb_bits, n_qkvg: int, n_fab: int,
@@ -167,8 +207,16 @@ def bf16_to_f64(bits) -> np.ndarray:
     return default().bf16_to_f64(bits)
 
 
+def fp16_to_f64(bits) -> np.ndarray:
+    return default().fp16_to_f64(bits)
+
+
 def f64_to_bf16(v) -> np.ndarray:
     return default().f64_to_bf16(v)
+
+
+def gemm_ex(x_bits, w_bits, res_bits=None, dtype: str = "bf16", nthreads: int = 1) -> np.ndarray:
+    return default().gemm_ex(x_bits, w_bits, res_bits, dtype, nthreads)
 
 
 def gemm(x_bits, w_bits, nthreads: int = 1) -> np.ndarray:
@@ -192,12 +240,27 @@ def ulp_bf16(v) -> np.ndarray:
     return np.where(a < 2.0 ** -126, 2.0 ** -133, u)
 
 
-def tolerance(ref, ulps: float = 4.0, abs_tol: float = 1e-3) -> np.ndarray:
-    """Per-element bound ``ulps * ulp_bf16(|ref|) + abs_tol``."""
-    return ulps * ulp_bf16(ref) + abs_tol
+def ulp_fp16(v) -> np.ndarray:
+    """fp16 unit in the last place at |v|: 2^(floor(log2|v|) - 10), 2^-24 below 2^-14."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    with np.errstate(divide="ignore"):
+        _, e = np.frexp(a)
+    E = e.astype(np.int64) - 1
+    u = np.ldexp(1.0, (E - 10).astype(np.int32))
+    return np.where(a < 2.0 ** -14, 2.0 ** -24, u)
 
 
-def compare(got, ref, ulps: float = 4.0, abs_tol: float = 1e-3, extra=None) -> dict:
+def ulp(v, dtype: str = "bf16") -> np.ndarray:
+    return {"bf16": ulp_bf16, "fp16": ulp_fp16}[dtype](v)
+
+
+def tolerance(ref, ulps: float = 4.0, abs_tol: float = 1e-3, dtype: str = "bf16") -> np.ndarray:
+    """Per-element bound ``ulps * ulp(|ref|) + abs_tol`` for outputs of type ``dtype``."""
+    return ulps * ulp(ref, dtype) + abs_tol
+
+
+def compare(got, ref, ulps: float = 4.0, abs_tol: float = 1e-3, extra=None,
+            dtype: str = "bf16") -> dict:
     """Element-wise check of ``got`` (float array) against ``ref`` (double).
 
     Non-finite values in ``got`` always fail. ``extra`` (optional, same shape)
@@ -208,7 +271,7 @@ def compare(got, ref, ulps: float = 4.0, abs_tol: float = 1e-3, extra=None) -> d
     r = np.asarray(ref, dtype=np.float64)
     if g.shape != r.shape:
         raise ValueError(f"shape mismatch {g.shape} vs {r.shape}")
-    bound = tolerance(r, ulps, abs_tol)
+    bound = tolerance(r, ulps, abs_tol, dtype)
     if extra is not None:
         bound = bound + np.asarray(extra, dtype=np.float64)
     finite = np.isfinite(g)

@@ -34,6 +34,14 @@
  * definition: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits;
  * subnormals down to 2^-133; round to nearest, ties to even.
  *
+ * The same page's kernel also takes fp16 inputs and an optional residual:
+ * C = A * B^T + residual, the residual (same element type, [M, N]) added to
+ * the fp32 accumulator after the K loop, before the single conversion to the
+ * output type. kdo_gemm_ex computes that in double: the K-sum as above, then
+ * one addition of the widened residual. fp16 is widened from the IEEE-754
+ * binary16 layout: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits,
+ * subnormals (exponent field 0) = fraction x 2^-24.
+ *
  * Build: gcc -O2 -fPIC -shared -pthread -ffp-contract=off (no fused
  * multiply-add contraction, no fast-math), so each product and each sum is a
  * separately rounded IEEE double operation on every host.
@@ -51,6 +59,29 @@ double kdo_bf16_to_f64(uint16_t b)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* fp16 bits -> double: (1024 + fraction) x 2^(exponent - 25) for a normal
+ * number, fraction x 2^-24 for a subnormal one (exponent field 0); exponent
+ * field 31 is infinity (fraction 0) or NaN. */
+double kdo_fp16_to_f64(uint16_t h)
+{
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x400), e - 25);
+    return (h & 0x8000) ? -v : v;
+}
+
+/* element widening for the two 16-bit input types: 0 = bf16, 1 = fp16 */
+static double widen(uint16_t b, int dtype)
+{
+    return dtype ? kdo_fp16_to_f64(b) : kdo_bf16_to_f64(b);
 }
 
 /* double -> bf16 bits, round to nearest, ties to even, with subnormals and
@@ -96,6 +127,12 @@ void kdo_widen_bf16(const uint16_t *in, double *out, int64_t n)
         out[i] = kdo_bf16_to_f64(in[i]);
 }
 
+void kdo_widen_fp16(const uint16_t *in, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = kdo_fp16_to_f64(in[i]);
+}
+
 /* ---- y = x * W^T, one output at a time, k ascending --------------------- */
 
 typedef struct {
@@ -103,9 +140,12 @@ typedef struct {
     int64_t ldx;
     const uint16_t *W;
     int64_t ldw;
+    const uint16_t *res;   /* NULL: no residual */
+    int64_t ldr;
+    int dtype;             /* 0 = bf16, 1 = fp16 (x, W and the residual) */
     double *y;
     int64_t ldy;
-    int M, K;
+    int M, N, K;
     int n_begin, n_end;
 } gemm_job;
 
@@ -117,9 +157,11 @@ static void gemm_columns(const gemm_job *j)
             const uint16_t *wr = j->W + (int64_t)n * j->ldw;
             double acc = 0.0;
             for (int k = 0; k < j->K; ++k) {
-                double p = kdo_bf16_to_f64(xr[k]) * kdo_bf16_to_f64(wr[k]);
+                double p = widen(xr[k], j->dtype) * widen(wr[k], j->dtype);
                 acc = acc + p;
             }
+            if (j->res)
+                acc = acc + widen(j->res[(int64_t)m * j->ldr + n], j->dtype);
             j->y[(int64_t)m * j->ldy + n] = acc;
         }
     }
@@ -132,14 +174,17 @@ static void *gemm_thread(void *arg)
 }
 
 /* x: [M, K] with row stride ldx elements; W: [N, K] with row stride ldw;
- * y: [M, N] doubles with row stride ldy. nthreads > 1 splits the N columns
- * into contiguous ranges, one per thread; every output is still computed by
- * one thread with the same loop, so the result does not depend on nthreads.
- * Returns 0, or -1 on a bad argument. */
-int kdo_gemm(const uint16_t *x, int64_t ldx, const uint16_t *W, int64_t ldw,
-             double *y, int64_t ldy, int M, int N, int K, int nthreads)
+ * res: NULL or [M, N] with row stride ldr; all three of type dtype (0 = bf16,
+ * 1 = fp16). y: [M, N] doubles with row stride ldy. nthreads > 1 splits the N
+ * columns into contiguous ranges, one per thread; every output is still
+ * computed by one thread with the same loop, so the result does not depend on
+ * nthreads. Returns 0, or -1 on a bad argument. */
+int kdo_gemm_ex(const uint16_t *x, int64_t ldx, const uint16_t *W, int64_t ldw,
+                const uint16_t *res, int64_t ldr, int dtype,
+                double *y, int64_t ldy, int M, int N, int K, int nthreads)
 {
-    if (M < 0 || N < 0 || K < 0 || ldx < K || ldw < K || ldy < N)
+    if (M < 0 || N < 0 || K < 0 || ldx < K || ldw < K || ldy < N || (res && ldr < N) ||
+        (dtype != 0 && dtype != 1))
         return -1;
     if (M == 0 || N == 0)
         return 0;
@@ -157,7 +202,8 @@ int kdo_gemm(const uint16_t *x, int64_t ldx, const uint16_t *W, int64_t ldw,
     for (int t = 0; t < nthreads; ++t) {
         gemm_job *j = &jobs[t];
         j->x = x; j->ldx = ldx; j->W = W; j->ldw = ldw;
-        j->y = y; j->ldy = ldy; j->M = M; j->K = K;
+        j->res = res; j->ldr = ldr; j->dtype = dtype;
+        j->y = y; j->ldy = ldy; j->M = M; j->N = N; j->K = K;
         j->n_begin = (int)(((int64_t)N * t) / nthreads);
         j->n_end = (int)(((int64_t)N * (t + 1)) / nthreads);
     }
@@ -176,6 +222,13 @@ int kdo_gemm(const uint16_t *x, int64_t ldx, const uint16_t *W, int64_t ldw,
     free(jobs);
     free(th);
     return 0;
+}
+
+/* bf16 inputs, no residual (the projections' GEMM). */
+int kdo_gemm(const uint16_t *x, int64_t ldx, const uint16_t *W, int64_t ldw,
+             double *y, int64_t ldy, int M, int N, int K, int nthreads)
+{
+    return kdo_gemm_ex(x, ldx, W, ldw, NULL, 0, 0, y, ldy, M, N, K, nthreads);
 }
 
 /* The full projection, in the page's order (see the header comment).

@@ -16,6 +16,11 @@ chained projection of "[Kimi-K3] Overlap low-M TP8 KDA projections"
 * brute force: exact rational sums on tiny shapes, against which the double
   oracle must sit within the summation error bound.
 
+The same page's kernel also takes fp16 inputs and adds an optional residual
+after the K loop (C = A * B^T + residual); ``gemm_ex`` is pinned by
+hand-derived fp16 decodings (``golden/fp16_decode_cases.txt``), an exact
+bit-field decode, closed forms with a residual and rational brute force.
+
 ``test_oracle_mutants.py`` runs every pin against deliberately broken copies
 of the oracle's C source to show each plausible mistake trips at least one.
 """
@@ -27,7 +32,7 @@ from fractions import Fraction
 import numpy as np
 import torch
 
-from decode_projection_gemms_gb300.inputs import bf16_bits, gen_w, gen_x
+from decode_projection_gemms_gb300.inputs import bf16_bits, bits16, gen_w, gen_x
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -43,6 +48,32 @@ def bf16_exact(bits: int) -> Fraction:
     else:
         v = Fraction(128 + f, 128) * (Fraction(2) ** (e - 127))
     return -v if s else v
+
+
+def fp16_exact(bits: int) -> Fraction:
+    """Exact value of a (finite) fp16 bit pattern, from its bit fields."""
+    s = (bits >> 15) & 1
+    e = (bits >> 10) & 0x1F
+    f = bits & 0x3FF
+    assert e != 0x1F, "not finite"
+    if e == 0:
+        v = Fraction(f, 1 << 24)
+    else:
+        v = Fraction(1024 + f, 1024) * (Fraction(2) ** (e - 15))
+    return -v if s else v
+
+
+def load_fp16_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "fp16_decode_cases.txt")) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            v = {"inf": float("inf"), "-inf": float("-inf"), "nan": float("nan")}.get(parts[1])
+            cases.append((int(parts[0], 16), float.fromhex(parts[1]) if v is None else v, line))
+    return cases
 
 
 def load_rne_cases():
@@ -65,6 +96,17 @@ def _const_bf16(shape, value: float) -> np.ndarray:
     t = torch.full(shape, value, dtype=torch.float32).to(torch.bfloat16)
     assert float(t.flatten()[0]) == value, "constant must be exact in bf16"
     return _bits(t)
+
+
+def _const(shape, value: float, dtype: str) -> np.ndarray:
+    tdt = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    t = torch.full(shape, value, dtype=torch.float32).to(tdt)
+    assert float(t.flatten()[0]) == value, f"constant must be exact in {dtype}"
+    return bits16(t)
+
+
+def _exact(bits: int, dtype: str) -> Fraction:
+    return bf16_exact(bits) if dtype == "bf16" else fp16_exact(bits)
 
 
 # ---- pins ---------------------------------------------------------------------
@@ -193,8 +235,87 @@ def pin_kda_slices(orc):
     assert np.array_equal(fb, orc.gemm(fa, wfb))
 
 
+def pin_fp16_golden(orc):
+    cases = load_fp16_cases()
+    bits = np.array([c[0] for c in cases], dtype=np.uint16)
+    got = orc.fp16_to_f64(bits)
+    for (b, want, line), g in zip(cases, got.tolist()):
+        if np.isnan(want):
+            assert np.isnan(g), f"fp16 {b:04X} -> {g!r}, want NaN  [{line}]"
+        else:
+            assert g == want and np.signbit(g) == np.signbit(want), \
+                f"fp16 {b:04X} -> {g!r}, want {want!r}  [{line}]"
+
+
+def pin_fp16_widen_exact(orc):
+    rng = np.random.default_rng(2)
+    bits = rng.integers(0, 1 << 16, size=4000, dtype=np.uint32).astype(np.uint16)
+    bits = bits[((bits >> 10) & 0x1F) != 0x1F]
+    got = orc.fp16_to_f64(bits)
+    for b, g in zip(bits.tolist(), got.tolist()):
+        assert Fraction(g) == fp16_exact(b), f"widen fp16 {b:04X} = {g!r}"
+
+
+def pin_gemm_ex_closed_forms(orc):
+    # all ones: K exactly; plus a residual r: K + r exactly (one addition)
+    for dtype in ("bf16", "fp16"):
+        for K in (1, 64, 1024, 7168):
+            x = _const((2, K), 1.0, dtype)
+            w = _const((3, K), 1.0, dtype)
+            assert np.array_equal(orc.gemm_ex(x, w, None, dtype), np.full((2, 3), float(K)))
+            r = np.stack([_const((3,), v, dtype) for v in (0.5, -3.0)])
+            y = orc.gemm_ex(x, w, r, dtype)
+            assert np.array_equal(y, np.array([[K + 0.5] * 3, [K - 3.0] * 3])), f"{dtype} K={K}: {y}"
+        # x = 0: the residual itself, element by element
+        M, N, K = 3, 5, 40
+        res = bits16(gen_x(M, N, seed=21, dtype=torch.float16 if dtype == "fp16" else torch.bfloat16))
+        y = orc.gemm_ex(_const((M, K), 0.0, dtype), _const((N, K), 1.0, dtype), res, dtype)
+        for m in range(M):
+            for n in range(N):
+                assert Fraction(float(y[m, n])) == _exact(int(res[m, n]), dtype), f"{dtype} y[{m},{n}]"
+
+
+def pin_fp16_one_hot(orc):
+    M, K, N = 3, 48, 10
+    w = bits16(gen_w(N, K, seed=13, std=1.0, dtype=torch.float16))
+    cols = [0, 47, 9]
+    xf = torch.zeros(M, K)
+    for m, j in enumerate(cols):
+        xf[m, j] = 1.0
+    y = orc.gemm_ex(bits16(xf.to(torch.float16)), w, None, "fp16")
+    for m, j in enumerate(cols):
+        for n in range(N):
+            assert Fraction(float(y[m, n])) == fp16_exact(int(w[n, j])), f"y[{m},{n}] != W[{n},{j}]"
+
+
+def pin_gemm_ex_brute_force(orc):
+    # exact rational sum + residual; the double result sits within
+    # gamma_{K+1} * (sum|x*w| + |r|) of it
+    u = Fraction(1, 1 << 53)
+    for dtype, tdt in (("bf16", torch.bfloat16), ("fp16", torch.float16)):
+        for (M, N, K, seed) in ((1, 2, 5, 0), (2, 3, 31, 1), (3, 2, 70, 2)):
+            x = bits16(gen_x(M, K, seed=300 + seed, dist="uniform", dtype=tdt))
+            w = bits16(gen_w(N, K, seed=400 + seed, std=1.0, dtype=tdt))
+            r = bits16(gen_x(M, N, seed=500 + seed, dtype=tdt))
+            y = orc.gemm_ex(x, w, r, dtype)
+            for m in range(M):
+                for n in range(N):
+                    terms = [_exact(int(x[m, k]), dtype) * _exact(int(w[n, k]), dtype) for k in range(K)]
+                    rv = _exact(int(r[m, n]), dtype)
+                    exact = sum(terms, Fraction(0)) + rv
+                    mag = sum((abs(t) for t in terms), Fraction(0)) + abs(rv)
+                    gamma = (K + 1) * u / (1 - (K + 1) * u)
+                    err = abs(Fraction(float(y[m, n])) - exact)
+                    assert err <= gamma * mag, f"{dtype} ({M},{N},{K}) y[{m},{n}] off by {float(err)}"
+
+
 PINS = [
     pin_rne_golden,
+    pin_fp16_golden,
+    pin_fp16_widen_exact,
+    pin_gemm_ex_closed_forms,
+    pin_fp16_one_hot,
+    pin_gemm_ex_brute_force,
     pin_widen_exact,
     pin_all_ones,
     pin_one_hot,
