@@ -14,7 +14,8 @@ values of the device time per call (us), median-free (total time / calls).
 Also reported: per-M us/call, HBM GB/s and roofline fraction (bytes =
 2(MK + NK + MN) summed over the three GEMMs), sequential vs overlapped times,
 the dominant kernel's roofline (Q/K/V/G GEMM timed alone), the CPU oracle on
-the host cores, the end-to-end number through host buffers, SM clocks.
+the host cores, the end-to-end number through host buffers, SM clocks, and
+skinny_gemm_ex (fp16 inputs, residual add) at the Q/K/V/G shape.
 
 --impl reference times the CPU oracle (the plain double-precision reference)
 on a bounded column sample of the same workload.
@@ -268,6 +269,7 @@ def run_ours(args):
         tot_one, _ = timed(graphs_one, args.cmp_steps)
         tot_q, _ = timed(graphs_q, args.cmp_steps)
     e2e = run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist)
+    ex = run_ex(args, wp_stack, dev, main, hbm_peak, dist)
     clock_info = clocks.stop()
 
     # reductions (max over ranks)
@@ -308,9 +310,17 @@ def run_ours(args):
                         for i, b in enumerate(("qkvg", "fab", "fb"))},
         }
     value = statistics.fmean(per_m[str(M)]["us_per_call"] for M in keys)
+    # our kernel launches per projection call in the timed mode: one for the
+    # single launch; Q/K/V/G + F_A/beta (+ F_B unless it is fused) otherwise
+    def launches_per_call(M):
+        if plan.overlap_at(M) == 2:
+            return 1
+        fused = plan.get_config(binding.BRANCH_FAB, M).flags & binding.FLAG_FUSE_FB
+        return 2 if fused else 3
     q_bytes = sum(qkvg_bytes(M) for M in keys)
     q_time_us = sum(per_m[str(M)]["qkvg_kernel_us"] for M in keys)
     achieved = q_bytes / (q_time_us * 1e3)  # GB/s
+    n_launches = args.steps * L * sum(launches_per_call(M) for M in keys)
     cpu = run_cpu_baseline(args, m_list) if (rank == 0 and not args.no_cpu) else None
     plan.close()
     if rank == 0:
@@ -342,12 +352,58 @@ def run_ours(args):
                          "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * len(keys) * L * 3,
+            "gpu_launches": n_launches,
+            "skinny_gemm_ex": ex,
             "clocks": clock_info,
         }
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
+
+
+def run_ex(args, wp_stack, dev, main, hbm_peak, dist, m_ex=(1, 16)):
+    """skinny_gemm_ex at the Q/K/V/G shape (N=4096, K=7168): bf16 and fp16
+    inputs, with and without a residual, each as a graph of one call per
+    layer of the rotated weight stack (device time per call)."""
+    import torch
+    from decode_projection_gemms_gb300 import binding
+    from decode_projection_gemms_gb300.inputs import gen_x
+
+    L = wp_stack.shape[0]
+    stacks = {"bf16": wp_stack[:, :N_QKVG], "fp16": wp_stack[:, :N_QKVG].to(torch.float16)}
+    out = {"shape": {"N": N_QKVG, "K": K}, "layers": L, "per_m": {}}
+    for M in m_ex:
+        row = {}
+        for dt, tdt in (("bf16", torch.bfloat16), ("fp16", torch.float16)):
+            x = gen_x(M, K, seed=0, dtype=tdt).to(dev)
+            r = gen_x(M, N_QKVG, seed=1, dtype=tdt).to(dev)
+            y = torch.empty((M, N_QKVG), dtype=tdt, device=dev)
+            for with_res in (False, True):
+                res = r if with_res else None
+                with torch.cuda.stream(main):
+                    binding.skinny_gemm_ex(x, stacks[dt][0], res, y)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=main):
+                    for layer in range(L):
+                        binding.skinny_gemm_ex(x, stacks[dt][layer], res, y)
+                with torch.cuda.stream(main):
+                    g.replay()
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(main)
+                    for _ in range(args.cmp_steps):
+                        g.replay()
+                    b.record(main)
+                torch.cuda.synchronize()
+                us = reduce_max([a.elapsed_time(b)], dist)[0] * 1e3 / (args.cmp_steps * L)
+                nbytes = qkvg_bytes(M) + (M * N_QKVG * 2 if with_res else 0)
+                key = dt + ("_residual" if with_res else "")
+                row[key] = {"us_per_call": round(us, 3), "gbs": round(nbytes / (us * 1e3), 1),
+                            "frac_of_roofline": round(nbytes / (us * 1e3) / hbm_peak, 4)}
+        out["per_m"][str(M)] = row
+    del stacks
+    return out
 
 
 def run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist):

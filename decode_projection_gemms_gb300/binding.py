@@ -28,6 +28,7 @@ KIND_AUTO, KIND_CC, KIND_TC05, KIND_SMALLK = 0, 1, 2, 3
 KIND_NAMES = {0: "auto", 1: "cc", 2: "tc05", 3: "smallk"}
 FLAG_PDL = 1
 FLAG_FUSE_FB = 2
+DTYPE_BF16, DTYPE_FP16 = 0, 1
 BRANCH_QKVG, BRANCH_FAB, BRANCH_FB = 0, 1, 2
 
 # exported symbols (must match include/kdaproj.h)
@@ -35,7 +36,7 @@ EXPORTS = (
     "skinny_gemm", "kp_select_config", "kp_table_load", "kp_table_clear", "kp_table_size",
     "kda_proj_plan", "kda_proj_set_overlap", "kda_proj_get_config", "kda_proj_set_config",
     "kda_proj_overlap_at", "kda_proj_run", "kda_proj_destroy", "kp_last_error", "kp_version",
-    "kp_device_error", "kp_scratch_bytes", "skinny_gemm_noalloc",
+    "kp_device_error", "kp_scratch_bytes", "skinny_gemm_noalloc", "skinny_gemm_ex",
 )
 
 
@@ -97,6 +98,7 @@ def load(path: str | None = None):
             "kp_device_error": [ctypes.POINTER(ci)],
             "kp_scratch_bytes": [ci, ci, ci, cfgp, ci, ctypes.POINTER(ctypes.c_size_t)],
             "skinny_gemm_noalloc": [vp, vp, vp, ci, ci, ci, cfgp, vp],
+            "skinny_gemm_ex": [vp, vp, vp, vp, ci, ci, ci, ci, cfgp, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -183,6 +185,49 @@ def skinny_gemm(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None,
     _check(load().skinny_gemm(x.data_ptr(), W.data_ptr(), y.data_ptr(), M, N, K,
                               ctypes.byref(cfg) if cfg is not None else None,
                               _stream_handle(stream)))
+    return y
+
+
+_DTYPES = {torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_FP16}
+
+
+def _half_2d(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in _DTYPES or (dtype is not None and t.dtype != dtype):
+        raise TypeError(f"{name} must be {dtype or 'bfloat16 or float16'}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D tensor")
+
+
+def skinny_gemm_ex(x: torch.Tensor, W: torch.Tensor, residual: torch.Tensor | None = None,
+                   y: torch.Tensor | None = None, cfg: KpCfg | None = None,
+                   stream=None) -> torch.Tensor:
+    """``y = round(x @ W.T + residual)`` with fp32 accumulation; x, W, residual
+    and y all bfloat16 or all float16 (the element type is x's). ``residual``
+    may be ``y`` itself."""
+    _half_2d(x, "x")
+    _half_2d(W, "W", x.dtype)
+    M, K = x.shape
+    N = W.shape[0]
+    if W.shape[1] != K:
+        raise ValueError(f"W has K={W.shape[1]}, x has K={K}")
+    if y is None:
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    _half_2d(y, "y", x.dtype)
+    if tuple(y.shape) != (M, N):
+        raise ValueError(f"y must be {(M, N)}")
+    if residual is not None:
+        _half_2d(residual, "residual", x.dtype)
+        if tuple(residual.shape) != (M, N):
+            raise ValueError(f"residual must be {(M, N)}")
+    _check(load().skinny_gemm_ex(x.data_ptr(), W.data_ptr(),
+                                 residual.data_ptr() if residual is not None else None,
+                                 y.data_ptr(), M, N, K, _DTYPES[x.dtype],
+                                 ctypes.byref(cfg) if cfg is not None else None,
+                                 _stream_handle(stream)))
     return y
 
 

@@ -21,8 +21,10 @@ LIB = os.path.join(BUILD, "libkdaproj.so")
 SOURCES = [
     "kp_api.cu",
     "kp_cc.cu",
-    "kp_cc_inst_lo.cu",
-    "kp_cc_inst_hi.cu",
+    "kp_cc_inst_lo_bf16.cu",
+    "kp_cc_inst_hi_bf16.cu",
+    "kp_cc_inst_lo_fp16.cu",
+    "kp_cc_inst_hi_fp16.cu",
     "kp_tc05.cu",
     "kp_smallk.cu",
     "kp_noalloc.cu",

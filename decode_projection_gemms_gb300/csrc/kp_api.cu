@@ -176,6 +176,7 @@ static cudaError_t launch_gemm(GemmArgs a, const kp_cfg &c, int sms, cudaStream_
             b.M = (M - m0) < 256 ? (M - m0) : 256;
             b.x = a.x + m0 * a.ldx;
             b.y = a.y + m0 * a.ldy;
+            b.res = a.res ? a.res + m0 * a.ldr : nullptr;
             cudaError_t e = tc05_launch(b, c, sms, s);
             if (e != cudaSuccess) return e;
         }
@@ -357,13 +358,22 @@ int kp_device_error(int *code) {
 
 int skinny_gemm(const void *x, const void *W, void *y, int M, int N, int K, const kp_cfg *cfg,
                 kp_stream_t stream) {
+    return skinny_gemm_ex(x, W, nullptr, y, M, N, K, KP_BF16, cfg, stream);
+}
+
+int skinny_gemm_ex(const void *x, const void *W, const void *residual, void *y, int M, int N,
+                   int K, int dtype, const kp_cfg *cfg, kp_stream_t stream) {
     if (M < 0 || N < 1 || K < 8)
         return set_error(KP_EINVAL, "skinny_gemm: bad sizes M=%d N=%d K=%d", M, N, K);
+    if (dtype != KP_BF16 && dtype != KP_FP16)
+        return set_error(KP_EINVAL, "skinny_gemm: unknown element type %d", dtype);
     if (K & 7) return set_error(KP_ESHAPE, "skinny_gemm: K=%d is not a multiple of 8", K);
     if (M == 0) return KP_OK;
     if (!x || !W || !y) return set_error(KP_EINVAL, "skinny_gemm: NULL pointer");
     if (!aligned16(x) || !aligned16(W) || !aligned16(y))
         return set_error(KP_EALIGN, "skinny_gemm: pointers must be 16-byte aligned");
+    if (residual && (reinterpret_cast<uintptr_t>(residual) & 1u))
+        return set_error(KP_EALIGN, "skinny_gemm: the residual must be 2-byte aligned");
     DevState *d = nullptr;
     int rc = device_state(&d);
     if (rc) return rc;
@@ -420,6 +430,9 @@ int skinny_gemm(const void *x, const void *W, void *y, int M, int N, int K, cons
     a.ws = d->ws;
     a.counters = d->cnt;
     a.err = d->err;
+    a.dtype = dtype;
+    a.res = static_cast<const uint16_t *>(residual);
+    a.ldr = N;
     cudaError_t e = launch_gemm(a, c, d->sms, stream);
     if (e != cudaSuccess) return cuda_fail(e, "skinny_gemm launch");
     return KP_OK;

@@ -18,10 +18,11 @@ int cc_variant(int R, int U) {
     return -1;
 }
 
-CCKernelFn cc_kernel(int M, int R, int U) {
+CCKernelFn cc_kernel(int M, int R, int U, int dtype) {
     const int v = cc_variant(R, U);
-    if (v < 0 || M < 1 || M > 16) return nullptr;
-    return M <= 8 ? cc_table_lo[M - 1][v] : cc_table_hi[M - 9][v];
+    if (v < 0 || M < 1 || M > 16 || (dtype != KP_BF16 && dtype != KP_FP16)) return nullptr;
+    if (dtype == KP_FP16) return M <= 8 ? cc_table_lo_fp16[M - 1][v] : cc_table_hi_fp16[M - 9][v];
+    return M <= 8 ? cc_table_lo_bf16[M - 1][v] : cc_table_hi_bf16[M - 9][v];
 }
 
 // K slice length: ceil(K / S) rounded up to 8 elements (16 bytes).
@@ -50,7 +51,7 @@ bool cc_supported(int M, int K, const kp_cfg &c) {
     if (M < 1 || M > 16 || K < 8 || (K & 7)) return false;
     if (c.split_k < 1 || c.split_k > K / 8) return false;
     if (c.block < 32 || c.block > 256 || (c.block & 31)) return false;
-    if (!cc_kernel(M, c.rows, c.k_unroll)) return false;
+    if (!cc_kernel(M, c.rows, c.k_unroll, KP_BF16)) return false;  // same set for fp16
     const int ks = cc_slice(K, c.split_k);
     return static_cast<long long>(M) * ks * 4 <= kMaxSmem;  // x slice fits in shared memory
 }
@@ -69,7 +70,8 @@ Scratch cc_scratch(int M, int N, int K, const kp_cfg &c) {
 
 cudaError_t cc_launch(const GemmArgs &a, const kp_cfg &c, cudaStream_t stream) {
     if (!cc_supported(a.M, a.K, c)) return cudaErrorInvalidValue;
-    CCKernelFn fn = cc_kernel(a.M, c.rows, c.k_unroll);
+    CCKernelFn fn = cc_kernel(a.M, c.rows, c.k_unroll, a.dtype);
+    if (!fn) return cudaErrorInvalidValue;
     CCParams p;
     p.a = a;
     p.Ks = cc_slice(a.K, c.split_k);

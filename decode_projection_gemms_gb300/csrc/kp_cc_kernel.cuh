@@ -1,6 +1,7 @@
 // CUDA-core split-K weight-streaming GEMV for M <= 16 tokens.
 //
-// y[m, n] = bf16( sum_k x[m, k] * W[n, k] ), fp32 accumulation: the skinny
+// y[m, n] = round( sum_k x[m, k] * W[n, k] (+ residual[m, n]) ), fp32
+// accumulation, bf16 or fp16 elements (template T): the skinny
 // GEMM of the Kimi K3 support page, part 1 (vllm PR #50089 digest, CuteSkinnyGemm, section
 // "关键源码片段"), whose design is prior art here: CUDA-core FMAs over 16-byte
 // vector loads, warp-shuffle row reductions, M unrolled at compile time.
@@ -8,7 +9,8 @@
 // so small-N shapes still fill all SMs, x's K slice is staged once per CTA in
 // shared memory as fp32, each warp owns `R` output rows, and the S partial
 // sums of a row tile are combined deterministically by the last CTA to finish
-// (ticket counter, sum in split order 0..S-1, one rounding to bf16).
+// (ticket counter, sum in split order 0..S-1, plus the residual if any, one
+// rounding to the element type).
 //
 // Grid: (row tiles, S). Block: `block` threads, warp w owns rows
 // tile*rows_cta + w*R .. +R-1. Lane l reads the 16-byte chunks l, l+32, ... of
@@ -27,7 +29,14 @@ struct CCParams {
     int rows_cta; // output rows per CTA
 };
 
-template <int M, int R, int U>
+// Store one output: the residual (if any) joins the fp32 sum, then one rounding.
+template <int T>
+__device__ __forceinline__ void cc_store(const GemmArgs &a, int m, int n, float v) {
+    if (a.res) v += elem_widen(a.res[m * a.ldr + n], T);
+    reinterpret_cast<uint16_t *>(a.y)[m * a.ldy + n] = elem_round<T>(v);
+}
+
+template <int M, int R, int U, int T>
 __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
     extern __shared__ float4 cc_smem[];
     float *xs = reinterpret_cast<float *>(cc_smem);  // [M][Ks] fp32
@@ -84,8 +93,8 @@ __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
                     for (int r = 0; r < R; ++r) {
                         const uint32_t w0 = h ? w[r][u].z : w[r][u].x;
                         const uint32_t w1 = h ? w[r][u].w : w[r][u].y;
-                        wf[r][0] = bf16lo(w0); wf[r][1] = bf16hi(w0);
-                        wf[r][2] = bf16lo(w1); wf[r][3] = bf16hi(w1);
+                        wf[r][0] = elem_lo<T>(w0); wf[r][1] = elem_hi<T>(w0);
+                        wf[r][2] = elem_lo<T>(w1); wf[r][3] = elem_hi<T>(w1);
                     }
 #pragma unroll
                     for (int m = 0; m < M; ++m) {
@@ -118,8 +127,8 @@ __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
         const int c = i - m * nchunk;
         const uint4 v = *reinterpret_cast<const uint4 *>(a.x + m * a.ldx + k0 + 8 * c);
         float4 *d = reinterpret_cast<float4 *>(xs + m * p.Ks + 8 * c);
-        d[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
-        d[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+        d[0] = make_float4(elem_lo<T>(v.x), elem_hi<T>(v.x), elem_lo<T>(v.y), elem_hi<T>(v.y));
+        d[1] = make_float4(elem_lo<T>(v.z), elem_hi<T>(v.z), elem_lo<T>(v.w), elem_hi<T>(v.w));
     }
     __syncthreads();
 
@@ -150,8 +159,7 @@ __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 const int n = row0 + r;
-                if (lane == ((r * M + m) & 31) && n < a.N)
-                    a.y[m * a.ldy + n] = __float2bfloat16_rn(acc[r][m]);
+                if (lane == ((r * M + m) & 31) && n < a.N) cc_store<T>(a, m, n, acc[r][m]);
             }
         return;
     }
@@ -195,7 +203,7 @@ __global__ void __launch_bounds__(256, 2) cc_gemv_kernel(const CCParams p) {
             for (int j = 0; j < 8; ++j)
                 if (q0 + j < p.S) t += v[j];
         }
-        a.y[m * a.ldy + n] = __float2bfloat16_rn(t);
+        cc_store<T>(a, m, n, t);
     }
     if (threadIdx.x == 0) a.counters[tile] = 0;  // ready for the next launch
 }
@@ -211,23 +219,27 @@ constexpr int kCCU[kCCVariants] = {4, 2, 4, 1, 2, 1};
 
 namespace kp {
 
-// Kernel pointer for (M, variant), or nullptr where the R*M accumulators
-// would not fit in the 128 registers a thread gets at two CTAs per SM.
-template <int M, int V>
+// Kernel pointer for (M, variant, element type), or nullptr where the R*M
+// accumulators would not fit in the 128 registers a thread gets at two CTAs
+// per SM.
+template <int M, int V, int T>
 constexpr CCKernelFn cc_pick() {
     if constexpr (kCCR[V] * M <= 64 && (kCCR[V] < 8 || M <= 4))
-        return cc_gemv_kernel<M, kCCR[V], kCCU[V]>;
+        return cc_gemv_kernel<M, kCCR[V], kCCU[V], T>;
     else
         return nullptr;
 }
 
-#define KP_CC_ROW(M)                                                                  \
-    {                                                                                 \
-        cc_pick<M, 0>(), cc_pick<M, 1>(), cc_pick<M, 2>(), cc_pick<M, 3>(),          \
-            cc_pick<M, 4>(), cc_pick<M, 5>()                                          \
+#define KP_CC_ROW(M, T)                                                                    \
+    {                                                                                      \
+        cc_pick<M, 0, T>(), cc_pick<M, 1, T>(), cc_pick<M, 2, T>(), cc_pick<M, 3, T>(),   \
+            cc_pick<M, 4, T>(), cc_pick<M, 5, T>()                                         \
     }
 
-extern const CCKernelFn cc_table_lo[8][kCCVariants];  // M = 1..8
-extern const CCKernelFn cc_table_hi[8][kCCVariants];  // M = 9..16
+// [M - 1 within the half][variant], one table per half and element type
+extern const CCKernelFn cc_table_lo_bf16[8][kCCVariants];  // M = 1..8
+extern const CCKernelFn cc_table_hi_bf16[8][kCCVariants];  // M = 9..16
+extern const CCKernelFn cc_table_lo_fp16[8][kCCVariants];
+extern const CCKernelFn cc_table_hi_fp16[8][kCCVariants];
 
 }  // namespace kp

@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,6 +24,12 @@ struct GemmArgs {
     float *ws;               // split-K partials (may be null if unused)
     int *counters;           // per-tile tickets, zero between launches
     int *err;                // device error word
+    // Element type of x, W, y and the residual (KP_BF16 or KP_FP16; the
+    // pointers above are raw 16-bit storage), and an optional residual
+    // [M, ldr] added to the fp32 sum before the one rounding.
+    int dtype = KP_BF16;
+    const uint16_t *res = nullptr;
+    int64_t ldr = 0;
 };
 
 // Scratch requirement of a configuration (floats and counters).
@@ -89,6 +96,37 @@ namespace kp {
 
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// The two 16-bit input types, as compile-time (T) or run-time (dtype)
+// choices: KP_BF16 or KP_FP16. lo/hi widen the low/high element of a 32-bit
+// word; round converts fp32 to the type's bits (round to nearest even).
+template <int T>
+__device__ __forceinline__ float elem_lo(uint32_t v) {
+    if constexpr (T == KP_FP16)
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+    else
+        return bf16lo(v);
+}
+template <int T>
+__device__ __forceinline__ float elem_hi(uint32_t v) {
+    if constexpr (T == KP_FP16)
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+    else
+        return bf16hi(v);
+}
+template <int T>
+__device__ __forceinline__ uint16_t elem_round(float f) {
+    if constexpr (T == KP_FP16)
+        return __half_as_ushort(__float2half_rn(f));
+    else
+        return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ float elem_widen(uint16_t b, int dtype) {
+    return dtype == KP_FP16 ? __half2float(__ushort_as_half(b)) : __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+__device__ __forceinline__ uint16_t elem_round(float f, int dtype) {
+    return dtype == KP_FP16 ? elem_round<KP_FP16>(f) : elem_round<KP_BF16>(f);
+}
 
 // Programmatic dependent launch. Without the launch attribute both are no-ops.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -1,4 +1,5 @@
-// CUDA-core small-K kernel: y = bf16(x * W^T) for K <= 256, the F_B shape
+// CUDA-core small-K kernel: y = round(x * W^T (+ residual)) for K <= 256,
+// bf16 or fp16 elements; the F_B shape
 // (out_fb[M, 1024] = f_a[M, 128] * W_fb^T, f_a read in place from the F_A/beta
 // output with row stride N_fab) of "[Kimi-K3] Overlap low-M TP8 KDA
 // projections" (run_fab_fb; _KdaSkinnyKGemm is the page's kernel for it and
@@ -21,6 +22,19 @@ namespace {
 constexpr int kMaxK = 256;
 constexpr int kMB = 32;  // tokens per pass
 
+// 8 elements of a 16-byte chunk, widened to fp32 into two float4.
+__device__ __forceinline__ void widen8(const uint4 v, int dtype, float4 *d) {
+    if (dtype == KP_FP16) {
+        d[0] = make_float4(elem_lo<KP_FP16>(v.x), elem_hi<KP_FP16>(v.x), elem_lo<KP_FP16>(v.y),
+                           elem_hi<KP_FP16>(v.y));
+        d[1] = make_float4(elem_lo<KP_FP16>(v.z), elem_hi<KP_FP16>(v.z), elem_lo<KP_FP16>(v.w),
+                           elem_hi<KP_FP16>(v.w));
+    } else {
+        d[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+        d[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+    }
+}
+
 __global__ void __launch_bounds__(256) smallk_kernel(const GemmArgs a, int rows_cta) {
     extern __shared__ float4 sk_smem[];
     const int K = a.K;
@@ -35,9 +49,7 @@ __global__ void __launch_bounds__(256) smallk_kernel(const GemmArgs a, int rows_
         const int r = i / kc;
         const int c = i - r * kc;
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.W + static_cast<int64_t>(n0 + r) * K + 8 * c));
-        float4 *d = reinterpret_cast<float4 *>(wsm + r * KP + 8 * c);
-        d[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
-        d[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+        widen8(v, a.dtype, reinterpret_cast<float4 *>(wsm + r * KP + 8 * c));
     }
     pdl_wait();
     pdl_trigger();
@@ -49,9 +61,7 @@ __global__ void __launch_bounds__(256) smallk_kernel(const GemmArgs a, int rows_
             const int mm = i / kc;
             const int c = i - mm * kc;
             const uint4 v = *reinterpret_cast<const uint4 *>(a.x + (m0 + mm) * a.ldx + 8 * c);
-            float4 *d = reinterpret_cast<float4 *>(xsm + mm * KP + 8 * c);
-            d[0] = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
-            d[1] = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+            widen8(v, a.dtype, reinterpret_cast<float4 *>(xsm + mm * KP + 8 * c));
         }
         __syncthreads();
         for (int idx = threadIdx.x; idx < rows_cta * mb; idx += blockDim.x) {
@@ -69,7 +79,9 @@ __global__ void __launch_bounds__(256) smallk_kernel(const GemmArgs a, int rows_
                 acc = fmaf(wv.z, xv.z, acc);
                 acc = fmaf(wv.w, xv.w, acc);
             }
-            a.y[(m0 + mm) * a.ldy + n0 + r] = __float2bfloat16_rn(acc);
+            const int m = m0 + mm;
+            if (a.res) acc += elem_widen(a.res[m * a.ldr + n0 + r], a.dtype);
+            reinterpret_cast<uint16_t *>(a.y)[m * a.ldy + n0 + r] = elem_round(acc, a.dtype);
         }
     }
 }

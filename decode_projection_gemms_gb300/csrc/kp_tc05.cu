@@ -1,4 +1,5 @@
-// TMA-fed tcgen05/TMEM cluster split-K kernel for y = bf16(x * W^T), M <= 256.
+// TMA-fed tcgen05/TMEM cluster split-K kernel for y = round(x * W^T (+ residual)),
+// bf16 or fp16 elements, M <= 256.
 //
 // The contraction is the skinny GEMM of the Kimi K3 support page, part 1
 // (vllm PR #50089 digest, CuteSkinnyGemm docstring: C = A * B^T, bf16 in,
@@ -64,6 +65,9 @@ struct Tc05Params {
     __nv_bfloat16 *y2;
     int64_t ldy2;
     int *err;
+    int dtype;                 // KP_BF16 / KP_FP16: operands, output and residual
+    const uint16_t *res;       // optional residual [M, ldr], added before the rounding
+    int64_t ldr;
     int M, N, Mpad;
     int KB;            // K blocks in K
     int C;             // CTAs per cluster = K splits per tile
@@ -96,11 +100,25 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t sbo) {
            (static_cast<uint64_t>(2) << 61);
 }
 
-__device__ __forceinline__ void store_y(const Tc05Params &p, int m, int n, __nv_bfloat16 v) {
+__device__ __forceinline__ void store_bits(const Tc05Params &p, int m, int n, uint16_t b) {
     if (n < p.n_split)
-        p.y[m * p.ldy + n] = v;
+        reinterpret_cast<uint16_t *>(p.y)[m * p.ldy + n] = b;
     else
-        p.y2[m * p.ldy2 + (n - p.n_split)] = v;
+        reinterpret_cast<uint16_t *>(p.y2)[m * p.ldy2 + (n - p.n_split)] = b;
+}
+
+// Output (m, n), n < N, of the general instantiation: the residual (if any)
+// joins the fp32 sum, one rounding to the element type, store; returns the
+// stored bits.
+__device__ __forceinline__ uint16_t finish(const Tc05Params &p, int m, int n, float v) {
+    if (p.res) v += elem_widen(p.res[m * p.ldr + n], p.dtype);
+    const uint16_t b = elem_round(v, p.dtype);
+    store_bits(p, m, n, b);
+    return b;
+}
+
+__device__ __forceinline__ uint16_t bf16_bits_rn(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
 // Byte offset of element (token m, feature k) of the fused F_B's B operand:
@@ -117,6 +135,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
         if (globaltimer_ns() - t0 > 1000000000ull) break;
 }
 
+// kGeneral = false: bf16 operands and output, no residual (the projections);
+// true: the element type and the residual come from the parameters.
+template <bool kGeneral>
 __global__ void __launch_bounds__(kThreads, 1)
     tc05_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                 const __grid_constant__ CUtensorMap tmx3, const __grid_constant__ CUtensorMap tmfb,
@@ -284,6 +305,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = tile * kTileN + row;
         __syncwarp();   // lane 0 may have been producing
         pdl_wait();
+        if constexpr (kGeneral) {
+            if (p.res) {
+                // Pull the residual this CTA adds at the end (its rows of the
+                // tile, every token) into L2 while the main loop runs.
+                const int rows = C == 1 ? kTileN : kTileN / C;
+                const int nr0 = tile * kTileN + (C == 1 ? 0 : rank * rows);
+                const int segs = (rows + 31) / 32;   // 64-byte pieces per token
+                for (int i = threadIdx.x - 64; i < p.M * segs; i += kThreads - 64) {
+                    const int m = i / segs;
+                    const int n = nr0 + (i - m * segs) * 32;
+                    if (n < p.N)
+                        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.res + m * p.ldr + n));
+                }
+            }
+        }
         mbar_wait_bounded(smem_u32(accf), 0, abort_flag, p.err, DEV_TIMEOUT_ACC_FULL);
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -298,11 +334,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (m < p.M) {
                     const float f = __uint_as_float(v[i]);
                     if (C == 1) {
-                        const __nv_bfloat16 b = __float2bfloat16_rn(f);
-                        if (n < p.N) store_y(p, m, n, b);
+                        uint16_t b;
+                        if constexpr (kGeneral) {
+                            b = n < p.N ? finish(p, m, n, f) : 0;
+                        } else {
+                            b = bf16_bits_rn(f);
+                            if (n < p.N) store_bits(p, m, n, b);
+                        }
                         if (fused)
-                            *reinterpret_cast<__nv_bfloat16 *>(gbase + p.off_bfa +
-                                                              bfa_offset(m, row, p.Mpad)) = b;
+                            *reinterpret_cast<uint16_t *>(gbase + p.off_bfa + bfa_offset(m, row, p.Mpad)) = b;
                     } else {
                         red[m * kTileN + row] = f;
                     }
@@ -338,21 +378,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc.w += part[c].w;
                 }
             const int nb = tile * kTileN + rr;
-            const __nv_bfloat16 b0 = __float2bfloat16_rn(acc.x);
-            const __nv_bfloat16 b1 = __float2bfloat16_rn(acc.y);
-            const __nv_bfloat16 b2 = __float2bfloat16_rn(acc.z);
-            const __nv_bfloat16 b3 = __float2bfloat16_rn(acc.w);
-            if (nb + 0 < p.N) store_y(p, m, nb + 0, b0);
-            if (nb + 1 < p.N) store_y(p, m, nb + 1, b1);
-            if (nb + 2 < p.N) store_y(p, m, nb + 2, b2);
-            if (nb + 3 < p.N) store_y(p, m, nb + 3, b3);
+            uint32_t b0, b1, b2, b3;
+            if constexpr (kGeneral) {
+                b0 = nb + 0 < p.N ? finish(p, m, nb + 0, acc.x) : 0;
+                b1 = nb + 1 < p.N ? finish(p, m, nb + 1, acc.y) : 0;
+                b2 = nb + 2 < p.N ? finish(p, m, nb + 2, acc.z) : 0;
+                b3 = nb + 3 < p.N ? finish(p, m, nb + 3, acc.w) : 0;
+            } else {
+                b0 = bf16_bits_rn(acc.x);
+                b1 = bf16_bits_rn(acc.y);
+                b2 = bf16_bits_rn(acc.z);
+                b3 = bf16_bits_rn(acc.w);
+                if (nb + 0 < p.N) store_bits(p, m, nb + 0, b0);
+                if (nb + 1 < p.N) store_bits(p, m, nb + 1, b1);
+                if (nb + 2 < p.N) store_bits(p, m, nb + 2, b2);
+                if (nb + 3 < p.N) store_bits(p, m, nb + 3, b3);
+            }
             if (fused) {
                 // this rank's features rr..rr+3 of the F_B operand (8 bytes)
-                __nv_bfloat162 lo, hi;
-                lo.x = b0; lo.y = b1; hi.x = b2; hi.y = b3;
-                uint2 pk;
-                pk.x = *reinterpret_cast<uint32_t *>(&lo);
-                pk.y = *reinterpret_cast<uint32_t *>(&hi);
+                const uint2 pk = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
                 *reinterpret_cast<uint2 *>(gbase + p.off_bfa + bfa_offset(m, rr, p.Mpad)) = pk;
             }
         }
@@ -479,8 +523,12 @@ cudaError_t get_encode(EncodeTiledFn *out) {
 
 // 2-D bf16 tensor map: `rows` x `cols` (cols contiguous, row stride `ld`
 // elements), box = box_rows x 64 columns, 128-byte swizzle, zero fill.
+CUtensorMapDataType map_type(int dtype) {
+    return dtype == KP_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+}
+
 cudaError_t make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int64_t ld,
-                     int box_rows) {
+                     int box_rows, int dtype = KP_BF16) {
     EncodeTiledFn enc;
     cudaError_t e = get_encode(&enc);
     if (e != cudaSuccess) return e;
@@ -488,7 +536,7 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int6
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+    CUresult r = enc(map, map_type(dtype), 2, const_cast<void *>(ptr), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -499,7 +547,7 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int6
 // element (i, r, b) is at r * ld + b * 64 + i. Box = 64 x box_rows x nkb, so
 // one copy lands nkb consecutive [box_rows][64] blocks. Needs cols % 64 == 0.
 cudaError_t make_map3(CUtensorMap *map, const void *ptr, int rows, int cols, int64_t ld,
-                      int box_rows, int nkb) {
+                      int box_rows, int nkb, int dtype) {
     EncodeTiledFn enc;
     cudaError_t e = get_encode(&enc);
     if (e != cudaSuccess) return e;
@@ -509,7 +557,7 @@ cudaError_t make_map3(CUtensorMap *map, const void *ptr, int rows, int cols, int
     cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), static_cast<cuuint32_t>(box_rows),
                          static_cast<cuuint32_t>(nkb)};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+    CUresult r = enc(map, map_type(dtype), 3, const_cast<void *>(ptr), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -613,6 +661,9 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     (void)num_sms;
     if (!tc05_supported(a.M, a.N, a.K, c)) return cudaErrorInvalidValue;
     if (fb && !tc05_fusable(a.M, c)) return cudaErrorInvalidValue;
+    // the fused F_B and the split output serve the bf16 projection only
+    if ((fb || split) && (a.dtype != KP_BF16 || a.res)) return cudaErrorInvalidValue;
+    if (a.dtype != KP_BF16 && a.dtype != KP_FP16) return cudaErrorInvalidValue;
     const int Mpad = mpad_of(a.M);
     const int nkb = nkb_of(c);
     const int stages = c.stages ? c.stages : max_stages(Mpad, nkb);
@@ -629,6 +680,9 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
         p.ldy2 = split->ldy2;
     }
     p.err = a.err;
+    p.dtype = a.dtype;
+    p.res = a.res;
+    p.ldr = a.ldr;
     p.M = a.M;
     p.N = a.N;
     p.Mpad = Mpad;
@@ -639,9 +693,11 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.stages = stages;
     p.n_tiles = (a.N + kTileN - 1) / kTileN;
     p.tile_rot = 0;
-    // kind::f16 instruction descriptor: D fp32 (bit 4), A and B bf16 (bits
-    // 7, 10), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-    p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(Mpad >> 3) << 17) |
+    // kind::f16 instruction descriptor: D fp32 (bit 4), A and B formats at
+    // bits 7 and 10 (1 = bf16, 0 = fp16), both K-major, N >> 3 at bit 17,
+    // M >> 4 at bit 24.
+    const uint32_t ab = a.dtype == KP_FP16 ? 0u : (1u << 7) | (1u << 10);
+    p.idesc = (1u << 4) | ab | (static_cast<uint32_t>(Mpad >> 3) << 17) |
               (static_cast<uint32_t>(kTileN >> 4) << 24);
     p.tmem_cols = tmem_cols_of(Mpad);
     p.stage_bytes = stage_bytes_of(Mpad, nkb);
@@ -668,13 +724,13 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     }
 
     CUtensorMap mw, mx, mx3;
-    cudaError_t e = make_map(&mw, a.W, a.N, a.K, a.K, kTileN);
+    cudaError_t e = make_map(&mw, a.W, a.N, a.K, a.K, kTileN, a.dtype);
     if (e != cudaSuccess) return e;
-    e = make_map(&mx, a.x, a.M, a.K, a.ldx, Mpad);
+    e = make_map(&mx, a.x, a.M, a.K, a.ldx, Mpad, a.dtype);
     if (e != cudaSuccess) return e;
     p.x3d = 0;
     memset(&mx3, 0, sizeof mx3);
-    if (a.K % kBlockK == 0 && nkb > 1 && make_map3(&mx3, a.x, a.M, a.K, a.ldx, Mpad, nkb) == cudaSuccess)
+    if (a.K % kBlockK == 0 && nkb > 1 && make_map3(&mx3, a.x, a.M, a.K, a.ldx, Mpad, nkb, a.dtype) == cudaSuccess)
         p.x3d = 1;
 
     int dev = 0;
@@ -683,10 +739,12 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_attr_devices.count(dev)) {
-            e = cudaFuncSetAttribute(tc05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kMaxSmem);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(tc05_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            for (auto fn : {tc05_kernel<false>, tc05_kernel<true>}) {
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            }
             if (e != cudaSuccess) return e;
             g_attr_devices.insert(dev);
         }
@@ -712,7 +770,9 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, tc05_kernel, mw, mx, mx3, mfb, p);
+    const bool general = a.dtype != KP_BF16 || a.res != nullptr;
+    return general ? cudaLaunchKernelEx(&cfg, tc05_kernel<true>, mw, mx, mx3, mfb, p)
+                   : cudaLaunchKernelEx(&cfg, tc05_kernel<false>, mw, mx, mx3, mfb, p);
 }
 
 }  // namespace kp

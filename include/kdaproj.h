@@ -86,6 +86,12 @@ enum kp_kind {
     KP_KIND_SMALLK = 3 /* CUDA-core small-K kernel (K <= 256), the F_B shape */
 };
 
+/* Element type of x, W, y and the residual in skinny_gemm_ex. */
+enum kp_dtype {
+    KP_BF16 = 0,
+    KP_FP16 = 1
+};
+
 enum kp_flags {
     KP_FLAG_PDL = 1,    /* launch with programmatic stream serialisation: the
                            kernel may start (and stream its weights) while the
@@ -135,6 +141,26 @@ typedef struct kda_plan kda_plan;
  * KP_ECUDA. */
 KP_API int skinny_gemm(const void *x, const void *W, void *y, int M, int N, int K,
                 const kp_cfg *cfg, kp_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * skinny_gemm_ex: y[M, N] = round(x[M, K] * W[N, K]^T + residual[M, N]), fp32
+ * accumulation, the residual (if any) widened to fp32 and added to the sum
+ * once after the K loop, then one rounding (to nearest even) to the element
+ * type. This is the skinny GEMM of the Kimi K3 support page, part 1 (vllm PR
+ * #50089 digest, CuteSkinnyGemm: C = A * B^T + residual with bf16 or fp16
+ * inputs and fp32 accumulation, the residual optional).
+ *   x, W, y   as for skinny_gemm, all of type dtype
+ *   residual  NULL, or device [M, N] row-major of type dtype, 2-byte aligned;
+ *             it may be y itself (each element is read before it is written,
+ *             by the same thread) but must not otherwise overlap y
+ *   dtype     KP_BF16 or KP_FP16
+ * Kernels, configurations, table lookup and scratch as for skinny_gemm (the
+ * table is keyed by shape only). skinny_gemm(x, W, y, ...) is
+ * skinny_gemm_ex(x, W, NULL, y, ..., KP_BF16, ...).
+ * Returns KP_OK, KP_EINVAL (also for an unknown dtype), KP_EALIGN, KP_ESHAPE,
+ * KP_ECONFIG, KP_ENODEV, KP_ECUDA. */
+KP_API int skinny_gemm_ex(const void *x, const void *W, const void *residual, void *y, int M,
+                          int N, int K, int dtype, const kp_cfg *cfg, kp_stream_t stream);
 
 /* Host-only: the configuration skinny_gemm would use for (M, N, K) on a
  * device with `num_sms` SMs (0 = query the current device). Lookup rounds M

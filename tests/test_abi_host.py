@@ -66,6 +66,13 @@ def test_argument_errors_need_no_device(lib):
     assert lib.kda_proj_plan(7168, 4096, 136, 1024, 0, ctypes.byref(out)) == binding.KP_EINVAL
     assert lib.kda_proj_destroy(None) == binding.KP_OK
     assert lib.kda_proj_set_overlap(None, 0) == binding.KP_ENOPLAN
+    # skinny_gemm_ex: element type and residual alignment, checked before any device work
+    assert lib.skinny_gemm_ex(p, p, None, p, 1, 8, 16, 2, None, None) == binding.KP_EINVAL
+    assert b"element type" in lib.kp_last_error()
+    assert lib.skinny_gemm_ex(p, p, ctypes.c_void_p(17), p, 1, 8, 16, binding.DTYPE_FP16,
+                              None, None) == binding.KP_EALIGN
+    assert lib.skinny_gemm_ex(p, p, None, p, 1, 8, 12, binding.DTYPE_FP16, None, None) == binding.KP_ESHAPE
+    assert lib.skinny_gemm_ex(p, p, p, p, 0, 8, 16, binding.DTYPE_FP16, None, None) == binding.KP_OK
 
 
 def test_builtin_rule(lib):
