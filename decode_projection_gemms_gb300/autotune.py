@@ -133,12 +133,48 @@ class Bench:
         return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
 
 
-def sweep_shape(M, N, K, sms, device, kinds, verbose=False):
+def sweep_candidates(M: int, N: int, K: int, sms: int):
+    """A short list for the shape sweep: the settings that decided the
+    projection shapes' tuning (grids of one to two CTAs per SM, split-K to fill
+    them, two K blocks per stage, as many stages as fit), around 10 per shape."""
+    out = []
+    if K <= 256:
+        out += [KpCfg.make("smallk", block=256, rows=r) for r in (8, 16)]
+    if M <= 16:
+        for (R, U) in ((1, 4), (2, 4), (4, 2)):
+            if R * M > 64:
+                continue
+            tiles = math.ceil(N / (8 * R))
+            for waves in (2, 4):
+                S = max(1, min(max(1, K // 256), round(waves * sms / tiles)))
+                out.append(KpCfg.make("cc", split_k=S, block=256, rows=R, k_unroll=U))
+    T = math.ceil(N / 128)
+    KB = math.ceil(K / 64)
+    Cs = [C for C in (1, 2, 4, 8, 16) if C <= KB and T * C <= 2 * sms]
+    for C in sorted(Cs, reverse=True)[:2]:
+        for P in (1, 2):
+            out.append(KpCfg.make("tc05", split_k=C, k_unroll=2, producers=P, stages=0))
+    valid, seen = [], set()
+    for c in out:
+        key = tuple(getattr(c, f) for f, _ in c._fields_)
+        if key in seen:
+            continue
+        seen.add(key)
+        try:
+            binding.scratch_bytes(M, N, K, c, sms)
+            valid.append(c)
+        except binding.KdaProjError:
+            pass
+    return valid
+
+
+def sweep_shape(M, N, K, sms, device, kinds, verbose=False, quick=False):
     b = Bench(M, N, K, device)
     results = []
-    for c in candidates(M, N, K, sms, kinds):
+    cands = sweep_candidates(M, N, K, sms) if quick else candidates(M, N, K, sms, kinds)
+    for c in cands:
         try:
-            us = b.time_cfg(c)
+            us = b.time_cfg(c, reps=5) if quick else b.time_cfg(c)
         except binding.KdaProjError as e:
             if verbose:
                 print(f"  skip {c.as_dict()}: {e}", file=sys.stderr)
@@ -314,6 +350,9 @@ def main(argv=None):
     ap.add_argument("--out", default=None)
     ap.add_argument("--json", default=None)
     ap.add_argument("--top", type=int, default=3)
+    ap.add_argument("--append-to", default=None,
+                    help="sweep: replace this table's lines for the swept (N, K) pairs with the "
+                         "new ones and write it back")
     ap.add_argument("-v", action="store_true")
     args = ap.parse_args(argv)
 
@@ -332,7 +371,8 @@ def main(argv=None):
         shapes = KDA_SHAPES
         ms = args.m or [1, 2, 4, 8, 16, 32, 64, 128]
     elif args.shapes == "sweep":
-        shapes = [(n, k) for n in SWEEP_N for k in SWEEP_K]
+        # the projection plan's own (N, K) pairs keep its jointly tuned entries
+        shapes = [(n, k) for n in SWEEP_N for k in SWEEP_K if (n, k) not in KDA_SHAPES]
         ms = args.m or SWEEP_M
     else:
         shapes = [tuple(int(v) for v in s.split(":")) for s in args.shapes.split(",")]
@@ -342,7 +382,7 @@ def main(argv=None):
     t0 = time.time()
     for (N, K) in shapes:
         for M in ms:
-            res = sweep_shape(M, N, K, sms, dev, kinds, args.v)
+            res = sweep_shape(M, N, K, sms, dev, kinds, args.v, quick=args.shapes == "sweep")
             if not res:
                 continue
             best_us, best = res[0]
@@ -352,6 +392,17 @@ def main(argv=None):
             print(lines[-1], flush=True)
     print(f"# sweep took {time.time() - t0:.1f} s", file=sys.stderr)
     _write(args, dev, sms, lines, dump)
+    if args.append_to:
+        swept = set(shapes)
+        keep = []
+        for line in open(args.append_to):
+            f = line.split("#")[0].split()
+            if len(f) >= 3 and (int(f[1]), int(f[2])) in swept:
+                continue
+            keep.append(line.rstrip("\n"))
+        with open(args.append_to, "w") as fh:
+            fh.write("\n".join(keep + [f"# shape sweep ({len(lines)} entries, "
+                                       f"{torch.cuda.get_device_name(dev)})"] + lines) + "\n")
 
 
 def _write(args, dev, sms, lines, dump):
