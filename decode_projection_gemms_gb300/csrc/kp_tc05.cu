@@ -55,6 +55,7 @@ constexpr int kBlockK = 64;            // K elements per block (128 bytes)
 constexpr uint32_t kWBlockBytes = kTileN * kBlockK * 2;  // 16 KB per K block
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kBarBytes = 512;
+constexpr int kMaxFbBufs = 8;          // W_fb tile buffers (one per F_B tile of a CTA)
 
 struct Tc05Params {
     __nv_bfloat16 *y;
@@ -85,7 +86,10 @@ struct Tc05Params {
     __nv_bfloat16 *yfb;
     int64_t ldfb;
     uint32_t off_bfa;  // shared-memory offset of the F_A operand [2][Mpad][128 B]
-    uint32_t off_wfb;  // shared-memory offset of one W_fb tile [2][128][128 B]
+    uint32_t off_wfb;  // shared-memory offset of the W_fb tile buffers, each [2][128][128 B]
+    int fb_bufs;       // W_fb tile buffers: all of a CTA's F_B tiles, or 1 (reused)
+    int fb_accs;       // TMEM accumulators the F_B tiles alternate between (1 or 2)
+    uint32_t tmem_cols_fb;  // TMEM columns of the fused tile's CTAs
     uint32_t idesc;
     uint32_t tmem_cols;
     uint32_t stage_bytes;
@@ -151,10 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(gbase + static_cast<size_t>(S) * p.stage_bytes);
     uint64_t *empty = full + S;
     uint64_t *accf = empty + S;
-    uint64_t *fbw = accf + 1;      // fused F_B: W_fb tile landed
-    uint64_t *fbacc = fbw + 1;     // fused F_B: accumulator ready
-    uint64_t *fbempty = fbacc + 1; // fused F_B: accumulator drained
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fbempty + 1);
+    uint64_t *fbw = accf + 1;                // fused F_B: W_fb tile landed, per buffer
+    uint64_t *fbacc = fbw + kMaxFbBufs;      // fused F_B: accumulator ready, per accumulator
+    uint64_t *fbempty = fbacc + 2;           // fused F_B: accumulator drained, per accumulator
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(fbempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -192,32 +196,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = pidx; j < kbs; j += P)
             tma_load_2d(st + j * kWBlockBytes, &tmw, bar, (k0 + j) * kBlockK, row0, pol_w);
     };
-    pdl_trigger();
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(smem_u32(full + s), static_cast<uint32_t>(p.producers));
             mbar_init(smem_u32(empty + s), 1);
         }
         mbar_init(smem_u32(accf), 1);
-        mbar_init(smem_u32(fbw), 1);
-        mbar_init(smem_u32(fbacc), 1);
-        mbar_init(smem_u32(fbempty), 4);
+        for (int i = 0; i < kMaxFbBufs; ++i) mbar_init(smem_u32(fbw + i), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(fbacc + i), 1);
+            mbar_init(smem_u32(fbempty + i), 4);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         // the weight stream starts before the TMEM allocation and the block barrier
         for (int s = 0; s < pre; ++s) issue_w(s, s, policy_evict_first());
         tma_prefetch_desc(&tmx);
         if (p.x3d) tma_prefetch_desc(&tmx3);
-        if (fused) tma_prefetch_desc(&tmfb);
+        if (fused) {
+            tma_prefetch_desc(&tmfb);
+            // W_fb does not depend on the previous kernel: pull this CTA's
+            // F_B weight tiles into L2 now, so their loads after the main
+            // loop hit it.
+            for (int i = 0; i < my_fb; ++i)
+                for (int j = 0; j < 2; ++j)
+                    tma_prefetch_l2_2d(&tmfb, j * kBlockK, (rank + i * C) * kTileN);
+        }
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+        tmem_alloc(smem_u32(tmem_slot), fused ? p.tmem_cols_fb : p.tmem_cols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Dependents may launch only once every CTA of this grid holds its TMEM:
+    // a dependent CTA that took the columns first would wait for this grid
+    // while this grid's allocation waited for it.
+    pdl_trigger();
 
     if (pidx >= 0 && lane == 0) {
         // ---------------- TMA producers ----------------
@@ -262,14 +279,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (pidx == 0 && my_fb > 0) {
             // The pipeline memory is free once every main-loop MMA has
-            // completed: fetch this CTA's first W_fb tile while the epilogue
-            // and the cluster reduction run.
+            // completed: fetch this CTA's W_fb tiles (as many as have a
+            // buffer) while the epilogue and the cluster reduction run.
             mbar_wait_bounded(smem_u32(accf), 0, abort_flag, p.err, DEV_TIMEOUT_ACC_FULL);
-            const uint32_t dst = base + p.off_wfb;
-            mbar_expect_tx(smem_u32(fbw), 2 * kWBlockBytes);
-            for (int j = 0; j < 2; ++j)
-                tma_load_2d(dst + j * kWBlockBytes, &tmfb, smem_u32(fbw), j * kBlockK,
-                            rank * kTileN, policy_evict_last());
+            const int nb = my_fb < p.fb_bufs ? my_fb : p.fb_bufs;
+            for (int i = 0; i < nb; ++i) {
+                const uint32_t dst = base + p.off_wfb + static_cast<uint32_t>(i) * 2 * kWBlockBytes;
+                mbar_expect_tx(smem_u32(fbw + i), 2 * kWBlockBytes);
+                for (int j = 0; j < 2; ++j)
+                    tma_load_2d(dst + j * kWBlockBytes, &tmfb, smem_u32(fbw + i), j * kBlockK,
+                                (rank + i * C) * kTileN, policy_evict_last());
+            }
         }
     }
     if (warp == 0) {
@@ -324,30 +344,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         float *red = reinterpret_cast<float *>(gbase);  // [Mpad][128] fp32, reuses stage memory
+        auto take = [&](int m, float f) {
+            if (C == 1) {
+                uint16_t b;
+                if constexpr (kGeneral) {
+                    b = n < p.N ? finish(p, m, n, f) : 0;
+                } else {
+                    b = bf16_bits_rn(f);
+                    if (n < p.N) store_bits(p, m, n, b);
+                }
+                if (fused)
+                    *reinterpret_cast<uint16_t *>(gbase + p.off_bfa + bfa_offset(m, row, p.Mpad)) = b;
+            } else {
+                red[m * kTileN + row] = f;
+            }
+        };
         for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(taddr + c0, v);
+            uint32_t va[16];
+            tmem_ld16(taddr + c0, va);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int m = c0 + i;
-                if (m < p.M) {
-                    const float f = __uint_as_float(v[i]);
-                    if (C == 1) {
-                        uint16_t b;
-                        if constexpr (kGeneral) {
-                            b = n < p.N ? finish(p, m, n, f) : 0;
-                        } else {
-                            b = bf16_bits_rn(f);
-                            if (n < p.N) store_bits(p, m, n, b);
-                        }
-                        if (fused)
-                            *reinterpret_cast<uint16_t *>(gbase + p.off_bfa + bfa_offset(m, row, p.Mpad)) = b;
-                    } else {
-                        red[m * kTileN + row] = f;
-                    }
-                }
-            }
+            for (int i = 0; i < 16; ++i)
+                if (c0 + i < p.M) take(c0 + i, __uint_as_float(va[i]));
         }
         tc_fence_before();
     }
@@ -395,34 +413,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nb + 3 < p.N) store_bits(p, m, nb + 3, b3);
             }
             if (fused) {
-                // this rank's features rr..rr+3 of the F_B operand (8 bytes)
+                // this rank's features rr..rr+3 of the F_B operand (8 bytes),
+                // written into its own copy and into every CTA of the cluster
+                // that computes F_B tiles (the F_B operand region lies past
+                // the partial tiles, so no reader is disturbed)
                 const uint2 pk = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+                const uint32_t off = base + p.off_bfa + bfa_offset(m, rr, p.Mpad);
                 *reinterpret_cast<uint2 *>(gbase + p.off_bfa + bfa_offset(m, rr, p.Mpad)) = pk;
+                for (int c = 0; c < C && c < p.fb_tiles; ++c)
+                    if (c != rank)
+                        asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(
+                                         mapa_shared(off, static_cast<uint32_t>(c))),
+                                     "r"(pk.x), "r"(pk.y)
+                                     : "memory");
             }
         }
-        // Peers may still be reading this CTA's partial tile.
+        // Written F_B operand slices reach the tensor cores' (async) proxy of
+        // whichever CTA reads them after the barrier.
+        if (fused) asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+        // Peers may still be reading this CTA's partial tile; after this
+        // barrier every F_B operand slice has landed everywhere.
         cluster_sync_all();
-        if (fused) {
-            // Gather the other ranks' F_A features (16-byte chunks of 8).
-            const int cpr = rpc / 8;  // chunks per rank
-            const int gather = my_fb > 0 ? p.M * 16 : 0;
-            for (int idx = threadIdx.x; idx < gather; idx += kThreads) {
-                const int m = idx >> 4;
-                const int c = idx & 15;
-                const int owner = c / cpr;
-                if (owner == rank) continue;
-                const uint32_t off = base + p.off_bfa + bfa_offset(m, c * 8, p.Mpad);
-                uint4 v;
-                asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                             : "r"(mapa_shared(off, static_cast<uint32_t>(owner)))
-                             : "memory");
-                *reinterpret_cast<uint4 *>(gbase + p.off_bfa + bfa_offset(m, c * 8, p.Mpad)) = v;
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            // everyone has copied everything it needs from its peers
-            cluster_sync_all();
-        }
     } else if (fused) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -432,48 +443,59 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (my_fb > 0) {
         // ---------------- fused F_B: out_fb = bf16(F_A) * W_fb^T ----------------
-        const uint32_t a_base = base + p.off_wfb;
+        // Tile i uses W_fb buffer i % B and TMEM accumulator i % A. Either
+        // every tile has its own buffer (B >= my_fb, loaded above), or B = 1
+        // and A = 1 and the buffer is refilled once the previous tile's MMAs
+        // are done.
+        const int B = p.fb_bufs;
+        const int A = p.fb_accs;
         const uint32_t b_base = base + p.off_bfa;
+        auto a_base = [&](int i) {
+            return base + p.off_wfb + static_cast<uint32_t>(i % B) * 2 * kWBlockBytes;
+        };
         if (warp == 0 && lane == 0) {
-            for (int i = 1; i < my_fb; ++i) {
+            for (int i = B; i < my_fb; ++i) {   // only with B = A = 1
                 mbar_wait_bounded(smem_u32(fbacc), static_cast<uint32_t>((i - 1) & 1), abort_flag,
                                   p.err, DEV_TIMEOUT_ACC_FULL);
                 mbar_expect_tx(smem_u32(fbw), 2 * kWBlockBytes);
                 for (int j = 0; j < 2; ++j)
-                    tma_load_2d(a_base + j * kWBlockBytes, &tmfb, smem_u32(fbw), j * kBlockK,
+                    tma_load_2d(a_base(i) + j * kWBlockBytes, &tmfb, smem_u32(fbw), j * kBlockK,
                                 (rank + i * C) * kTileN, policy_evict_last());
             }
         } else if (warp == 1 && lane == 0) {
             tc_fence_after();
             for (int i = 0; i < my_fb; ++i) {
-                if (i > 0)
-                    mbar_wait_bounded(smem_u32(fbempty), static_cast<uint32_t>((i - 1) & 1),
+                const int a = i % A;
+                if (i >= A)
+                    mbar_wait_bounded(smem_u32(fbempty + a), static_cast<uint32_t>(((i - A) / A) & 1),
                                       abort_flag, p.err, DEV_TIMEOUT_ACC_EMPTY);
-                mbar_wait_bounded(smem_u32(fbw), static_cast<uint32_t>(i & 1), abort_flag, p.err,
-                                  DEV_TIMEOUT_FULL);
+                mbar_wait_bounded(smem_u32(fbw + i % B), static_cast<uint32_t>((i / B) & 1), abort_flag,
+                                  p.err, DEV_TIMEOUT_FULL);
                 tc_fence_after();
                 for (int j = 0; j < 2; ++j) {
-                    const uint64_t ad = smem_desc(a_base + j * kWBlockBytes, 1024);
+                    const uint64_t ad = smem_desc(a_base(i) + j * kWBlockBytes, 1024);
                     const uint64_t bd = smem_desc(b_base + j * p.Mpad * 128, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk)
-                        umma_bf16(tmem_base, ad + 2 * kk, bd + 2 * kk, p.idesc,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16(tmem_base + static_cast<uint32_t>(a * p.Mpad), ad + 2 * kk, bd + 2 * kk,
+                                  p.idesc, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                umma_commit(smem_u32(fbacc));
+                umma_commit(smem_u32(fbacc + a));
             }
         } else if (warp >= 2) {
             const int q = warp & 3;
             const int row = q * 32 + lane;
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
             for (int i = 0; i < my_fb; ++i) {
-                mbar_wait_bounded(smem_u32(fbacc), static_cast<uint32_t>(i & 1), abort_flag, p.err,
-                                  DEV_TIMEOUT_ACC_FULL);
+                const int a = i % A;
+                mbar_wait_bounded(smem_u32(fbacc + a), static_cast<uint32_t>((i / A) & 1), abort_flag,
+                                  p.err, DEV_TIMEOUT_ACC_FULL);
                 tc_fence_after();
                 const int n = (rank + i * C) * kTileN + row;
+                const uint32_t tcol = taddr + static_cast<uint32_t>(a * p.Mpad);
                 for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
                     uint32_t v[16];
-                    tmem_ld16(taddr + c0, v);
+                    tmem_ld16(tcol + c0, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
@@ -484,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(fbempty));
+                if (lane == 0) mbar_arrive(smem_u32(fbempty + a));
             }
         }
     }
@@ -492,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+    if (warp == 1) tmem_dealloc(tmem_base, fused ? p.tmem_cols_fb : p.tmem_cols);
 }
 
 // ---- host helpers -------------------------------------------------------------
@@ -637,12 +659,12 @@ Scratch tc05_scratch(int, int, int, const kp_cfg &, int) { return Scratch(); }
 namespace {
 // Shared-memory layout of the fused F_B after the main loop (offsets from the
 // 1024-aligned base): [partial tile Mpad x 128 fp32][F_A operand 2 x Mpad x
-// 128 B][one W_fb tile 2 x 16 KB]. It must fit in the pipeline memory.
-void fb_layout(int Mpad, uint32_t *off_bfa, uint32_t *off_wfb, uint32_t *end) {
+// 128 B][nbuf W_fb tiles of 2 x 16 KB]. It must fit in the pipeline memory.
+void fb_layout(int Mpad, uint32_t *off_bfa, uint32_t *off_wfb, uint32_t *end, int nbuf = 1) {
     auto al = [](uint32_t v) { return (v + 1023u) & ~1023u; };
     *off_bfa = al(static_cast<uint32_t>(Mpad) * kTileN * 4);
     *off_wfb = al(*off_bfa + static_cast<uint32_t>(Mpad) * 256);
-    *end = *off_wfb + 2 * kWBlockBytes;
+    *end = *off_wfb + static_cast<uint32_t>(nbuf) * 2 * kWBlockBytes;
 }
 }  // namespace
 
@@ -708,11 +730,24 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.yfb = nullptr;
     p.ldfb = 0;
     p.off_bfa = p.off_wfb = 0;
+    p.fb_bufs = 1;
+    p.fb_accs = 1;
+    p.tmem_cols_fb = p.tmem_cols;
     CUtensorMap mfb;
     memset(&mfb, 0, sizeof mfb);
     if (fb) {
         uint32_t end;
         fb_layout(Mpad, &p.off_bfa, &p.off_wfb, &end);
+        // a buffer per F_B tile of a CTA when they fit (else one, refilled),
+        // and two TMEM accumulators when a CTA has several tiles
+        const int tiles = (fb->N + kTileN - 1) / kTileN;
+        const int per_cta = (tiles + p.C - 1) / p.C;
+        const size_t pipe = static_cast<size_t>(stages) * stage_bytes_of(Mpad, nkb);
+        uint32_t ob, ow, end_all;
+        fb_layout(Mpad, &ob, &ow, &end_all, per_cta);
+        p.fb_bufs = (per_cta <= kMaxFbBufs && end_all <= pipe) ? per_cta : 1;
+        p.fb_accs = (p.fb_bufs >= per_cta && per_cta > 1 && 2 * Mpad <= 256) ? 2 : 1;
+        p.tmem_cols_fb = tmem_cols_of(p.fb_accs * Mpad);
         p.fb_tile = fb->tile;
         p.tile_rot = fb->tile;
         p.N_fb = fb->N;
@@ -754,7 +789,24 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(T * p.C, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem_of(Mpad, nkb, stages);
+    // TMEM is 512 columns per SM and an allocation that does not fit waits;
+    // CTAs of a cluster wait for each other, so the CTAs that can share an SM
+    // must never need more than 512 columns together. Shared memory bounds
+    // what shares an SM: each CTA takes at least cols/512 of the SM's shared
+    // memory (with its per-block reserve), so any mix of such CTAs fits.
+    size_t smem = smem_of(Mpad, nkb, stages);
+    {
+        const uint32_t cols = p.tmem_cols_fb > p.tmem_cols ? p.tmem_cols_fb : p.tmem_cols;
+        int sm_smem = 0, reserved = 0;
+        if (cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+            return cudaErrorInvalidValue;
+        const long long need =
+            (static_cast<long long>(sm_smem) * cols + 511) / 512 - reserved;
+        if (need > static_cast<long long>(smem)) smem = static_cast<size_t>(need);
+        if (smem > static_cast<size_t>(kMaxSmem)) return cudaErrorInvalidValue;
+    }
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
