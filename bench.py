@@ -59,14 +59,16 @@ def qkvg_bytes(M: int) -> int:
     return 2 * (M * K + N_QKVG * K + M * N_QKVG)
 
 
-def load_peaks():
+def load_peaks(burst: bool = False):
+    """(HBM GB/s, bf16 TFLOP/s, source): the sustained tensor figure for the
+    long decode step, the burst one for a kernel timed alone."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         d = json.load(open(p))
-        return (float(d["hbm_gbs"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
-                "measured")
+        tc = d["bf16_tflops"] if burst else d.get("bf16_tflops_sustained", d["bf16_tflops"])
+        return float(d["hbm_gbs"]), float(tc), "measured"
     except Exception:
-        return 6800.0, 1700.0, "fallback"
+        return 6800.0, 1900.0 if burst else 1700.0, "fallback"
 
 
 # ---------------------------------------------------------------------------
@@ -178,6 +180,7 @@ def run_ours(args):
     barrier(dist)
     binding.load()
     hbm_peak, tc_peak, peak_src = load_peaks()
+    tc_peak_burst = load_peaks(burst=True)[1]
     m_list = args.m or [m for m in M_LIST if m <= args.max_m]
     L = args.layers
 
@@ -270,6 +273,7 @@ def run_ours(args):
         tot_q, _ = timed(graphs_q, args.cmp_steps)
     e2e = run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist)
     ex = run_ex(args, wp_stack, dev, main, hbm_peak, dist)
+    prefill = run_prefill(args, wp_stack, dev, main, tc_peak_burst, dist)
     clock_info = clocks.stop()
 
     # reductions (max over ranks)
@@ -354,6 +358,7 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": n_launches,
             "skinny_gemm_ex": ex,
+            "prefill": prefill,
             "clocks": clock_info,
         }
         print(json.dumps(line))
@@ -403,6 +408,57 @@ def run_ex(args, wp_stack, dev, main, hbm_peak, dist, m_ex=(1, 16)):
                             "frac_of_roofline": round(nbytes / (us * 1e3) / hbm_peak, 4)}
         out["per_m"][str(M)] = row
     del stacks
+    return out
+
+
+def run_prefill(args, wp_stack, dev, main, tc_peak, dist, m_pre=(256, 1024, 4096), layers=8):
+    """skinny_gemm at prefill token counts on the Q/K/V/G weights (N=4096,
+    K=7168): one tcgen05 launch per call with token tiles of 256 on the grid,
+    against calling it once per 256-token slice (which streams the weights
+    from HBM once per slice). Device time per call, TFLOP/s."""
+    import torch
+    from decode_projection_gemms_gb300 import binding
+    from decode_projection_gemms_gb300.inputs import gen_x
+
+    L = min(layers, wp_stack.shape[0])
+    out = {"shape": {"N": N_QKVG, "K": K}, "layers": L, "per_m": {}}
+    for M in m_pre:
+        x = gen_x(M, K, seed=2).to(dev)
+        y = torch.empty((M, N_QKVG), dtype=torch.bfloat16, device=dev)
+
+        def call(layer, sliced):
+            w = wp_stack[layer, :N_QKVG]
+            if not sliced:
+                binding.skinny_gemm(x, w, y)
+            else:
+                for m0 in range(0, M, 256):
+                    binding.skinny_gemm(x[m0:m0 + 256], w, y[m0:m0 + 256])
+
+        row = {}
+        for sliced in (False, True):
+            with torch.cuda.stream(main):
+                call(0, sliced)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=main):
+                for layer in range(L):
+                    call(layer, sliced)
+            reps = max(2, args.cmp_steps // 4)
+            with torch.cuda.stream(main):
+                g.replay()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(main)
+                for _ in range(reps):
+                    g.replay()
+                b.record(main)
+            torch.cuda.synchronize()
+            us = reduce_max([a.elapsed_time(b)], dist)[0] * 1e3 / (reps * L)
+            tf = 2.0 * M * N_QKVG * K / (us * 1e6)
+            row["per_256_slices" if sliced else "one_launch"] = {
+                "us_per_call": round(us, 2), "tflops": round(tf, 1),
+                "frac_of_tensor_peak": round(tf / tc_peak, 4)}
+        out["per_m"][str(M)] = row
     return out
 
 

@@ -164,24 +164,13 @@ static Scratch scratch_of(int M, int N, int K, const kp_cfg &c, int sms) {
     }
 }
 
-// Launch one GEMM with configuration c; TC05 processes M in 256-row slices.
+// Launch one GEMM with configuration c (TC05 covers any M in one launch:
+// token tiles of 256 along the grid's y axis).
 static cudaError_t launch_gemm(GemmArgs a, const kp_cfg &c, int sms, cudaStream_t s) {
     switch (c.kind) {
     case KP_KIND_CC: return cc_launch(a, c, s);
     case KP_KIND_SMALLK: return smallk_launch(a, c, s);
-    case KP_KIND_TC05: {
-        const int M = a.M;
-        for (int m0 = 0; m0 < M; m0 += 256) {
-            GemmArgs b = a;
-            b.M = (M - m0) < 256 ? (M - m0) : 256;
-            b.x = a.x + m0 * a.ldx;
-            b.y = a.y + m0 * a.ldy;
-            b.res = a.res ? a.res + m0 * a.ldr : nullptr;
-            cudaError_t e = tc05_launch(b, c, sms, s);
-            if (e != cudaSuccess) return e;
-        }
-        return cudaSuccess;
-    }
+    case KP_KIND_TC05: return tc05_launch(a, c, sms, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -1,5 +1,6 @@
 // TMA-fed tcgen05/TMEM cluster split-K kernel for y = round(x * W^T (+ residual)),
-// bf16 or fp16 elements, M <= 256.
+// bf16 or fp16 elements, any M: up to 256 tokens per CTA (the MMA's N), more
+// tokens as further token tiles along the grid's y axis of the same launch.
 //
 // The contraction is the skinny GEMM of the Kimi K3 support page, part 1
 // (vllm PR #50089 digest, CuteSkinnyGemm docstring: C = A * B^T, bf16 in,
@@ -141,7 +142,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 // kGeneral = false: bf16 operands and output, no residual (the projections);
 // true: the element type and the residual come from the parameters.
-template <bool kGeneral>
+// kTiled = false: one token tile (M <= 256); true: token tiles along the
+// grid's y axis.
+template <bool kGeneral, bool kTiled>
 __global__ void __launch_bounds__(kThreads, 1)
     tc05_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                 const __grid_constant__ CUtensorMap tmx3, const __grid_constant__ CUtensorMap tmfb,
@@ -169,6 +172,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // longest epilogue.
     const int tile = (static_cast<int>(blockIdx.x) / C + p.tile_rot) % p.n_tiles;
     const bool fused = (p.fb_tile >= 0 && tile == p.fb_tile);
+    // Token tile of this CTA: tokens [m0, m0 + Mloc). All token tiles of a
+    // feature tile run together, so its weights come from HBM once and from
+    // L2 for the other token tiles.
+    const int m0 = kTiled ? static_cast<int>(blockIdx.y) * p.Mpad : 0;
+    const int Mloc = kTiled ? min(p.M - m0, p.Mpad) : p.M;
     const int kb0 = static_cast<int>((static_cast<long long>(p.KB) * rank) / C);
     const int kb1 = static_cast<int>((static_cast<long long>(p.KB) * (rank + 1)) / C);
     const int n_st = (kb1 - kb0 + p.nkb - 1) / p.nkb;  // stages of work for this CTA
@@ -249,10 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t st = base + stage * p.stage_bytes + p.w_stage_bytes;
             const uint32_t bar = smem_u32(full + stage);
             if (x_full(kbs)) {
-                tma_load_3d(st, &tmx3, bar, 0, 0, k0, pol_x);
+                tma_load_3d(st, &tmx3, bar, 0, m0, k0, pol_x);
             } else {
                 for (int j = 0; j < kbs; ++j)
-                    tma_load_2d(st + j * xblk, &tmx, bar, (k0 + j) * kBlockK, 0, pol_x);
+                    tma_load_2d(st + j * xblk, &tmx, bar, (k0 + j) * kBlockK, m0, pol_x);
             }
         };
         // Weights never depend on the previous kernel: the first stages' W
@@ -332,11 +340,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rows = C == 1 ? kTileN : kTileN / C;
                 const int nr0 = tile * kTileN + (C == 1 ? 0 : rank * rows);
                 const int segs = (rows + 31) / 32;   // 64-byte pieces per token
-                for (int i = threadIdx.x - 64; i < p.M * segs; i += kThreads - 64) {
+                for (int i = threadIdx.x - 64; i < Mloc * segs; i += kThreads - 64) {
                     const int m = i / segs;
                     const int n = nr0 + (i - m * segs) * 32;
                     if (n < p.N)
-                        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.res + m * p.ldr + n));
+                        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.res + (m0 + m) * p.ldr + n));
                 }
             }
         }
@@ -348,10 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (C == 1) {
                 uint16_t b;
                 if constexpr (kGeneral) {
-                    b = n < p.N ? finish(p, m, n, f) : 0;
+                    b = n < p.N ? finish(p, m0 + m, n, f) : 0;
                 } else {
                     b = bf16_bits_rn(f);
-                    if (n < p.N) store_bits(p, m, n, b);
+                    if (n < p.N) store_bits(p, m0 + m, n, b);
                 }
                 if (fused)
                     *reinterpret_cast<uint16_t *>(gbase + p.off_bfa + bfa_offset(m, row, p.Mpad)) = b;
@@ -365,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                if (c0 + i < p.M) take(c0 + i, __uint_as_float(va[i]));
+                if (c0 + i < Mloc) take(c0 + i, __uint_as_float(va[i]));
         }
         tc_fence_before();
     }
@@ -378,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int groups = rpc / 4;             // float4 groups per token
         const int r0 = rank * rpc;
         const uint32_t red_base = base;         // same offset in every CTA
-        for (int idx = threadIdx.x; idx < p.M * groups; idx += kThreads) {
+        for (int idx = threadIdx.x; idx < Mloc * groups; idx += kThreads) {
             const int m = idx / groups;
             const int rr = r0 + 4 * (idx - m * groups);
             const uint32_t off = red_base + static_cast<uint32_t>((m * kTileN + rr) * 4);
@@ -398,19 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nb = tile * kTileN + rr;
             uint32_t b0, b1, b2, b3;
             if constexpr (kGeneral) {
-                b0 = nb + 0 < p.N ? finish(p, m, nb + 0, acc.x) : 0;
-                b1 = nb + 1 < p.N ? finish(p, m, nb + 1, acc.y) : 0;
-                b2 = nb + 2 < p.N ? finish(p, m, nb + 2, acc.z) : 0;
-                b3 = nb + 3 < p.N ? finish(p, m, nb + 3, acc.w) : 0;
+                b0 = nb + 0 < p.N ? finish(p, m0 + m, nb + 0, acc.x) : 0;
+                b1 = nb + 1 < p.N ? finish(p, m0 + m, nb + 1, acc.y) : 0;
+                b2 = nb + 2 < p.N ? finish(p, m0 + m, nb + 2, acc.z) : 0;
+                b3 = nb + 3 < p.N ? finish(p, m0 + m, nb + 3, acc.w) : 0;
             } else {
                 b0 = bf16_bits_rn(acc.x);
                 b1 = bf16_bits_rn(acc.y);
                 b2 = bf16_bits_rn(acc.z);
                 b3 = bf16_bits_rn(acc.w);
-                if (nb + 0 < p.N) store_bits(p, m, nb + 0, b0);
-                if (nb + 1 < p.N) store_bits(p, m, nb + 1, b1);
-                if (nb + 2 < p.N) store_bits(p, m, nb + 2, b2);
-                if (nb + 3 < p.N) store_bits(p, m, nb + 3, b3);
+                if (nb + 0 < p.N) store_bits(p, m0 + m, nb + 0, b0);
+                if (nb + 1 < p.N) store_bits(p, m0 + m, nb + 1, b1);
+                if (nb + 2 < p.N) store_bits(p, m0 + m, nb + 2, b2);
+                if (nb + 3 < p.N) store_bits(p, m0 + m, nb + 3, b3);
             }
             if (fused) {
                 // this rank's features rr..rr+3 of the F_B operand (8 bytes),
@@ -500,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const int m = c0 + e;
-                        if (m < p.M && n < p.N_fb)
+                        if (m < Mloc && n < p.N_fb)
                             p.yfb[m * p.ldfb + n] = __float2bfloat16_rn(__uint_as_float(v[e]));
                     }
                 }
@@ -586,7 +594,8 @@ cudaError_t make_map3(CUtensorMap *map, const void *ptr, int rows, int cols, int
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int mpad_of(int M) { return (M + 15) & ~15; }
+// Tokens per CTA (the MMA's N): M padded to 16, at most 256 (one token tile).
+int mpad_of(int M) { return ((M < 256 ? M : 256) + 15) & ~15; }
 
 uint32_t w_stage_bytes_of(int nkb) { return static_cast<uint32_t>(nkb) * kWBlockBytes; }
 
@@ -623,9 +632,10 @@ kp_cfg tc05_default(int M, int N, int K, int num_sms) {
     c.flags = KP_FLAG_PDL;
     const int T = (N + kTileN - 1) / kTileN;
     const int KB = (K + kBlockK - 1) / kBlockK;
+    const int mt = (M + 255) / 256;   // token tiles
     int C = 1;
-    while (C < 16 && T * C * 2 <= num_sms && C * 2 <= KB) C *= 2;
-    const int Mpad = mpad_of(M < 256 ? M : 256);
+    while (C < 16 && T * mt * C * 2 <= num_sms && C * 2 <= KB) C *= 2;
+    const int Mpad = mpad_of(M);
     int nkb = 4;
     while (nkb > 1 && max_stages(Mpad, nkb) < 3) nkb /= 2;
     c.split_k = C;
@@ -636,7 +646,8 @@ kp_cfg tc05_default(int M, int N, int K, int num_sms) {
 }
 
 bool tc05_supported(int M, int N, int K, const kp_cfg &c) {
-    if (M < 1 || M > 256 || N < 1 || K < 8 || (K & 7)) return false;
+    if (M < 1 || N < 1 || K < 8 || (K & 7)) return false;
+    if ((M + 255) / 256 > 65535) return false;   // token tiles along the grid's y axis
     const int C = cluster_of(c);
     if (C != 1 && C != 2 && C != 4 && C != 8 && C != 16) return false;
     const int KB = (K + kBlockK - 1) / kBlockK;
@@ -684,7 +695,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     if (!tc05_supported(a.M, a.N, a.K, c)) return cudaErrorInvalidValue;
     if (fb && !tc05_fusable(a.M, c)) return cudaErrorInvalidValue;
     // the fused F_B and the split output serve the bf16 projection only
-    if ((fb || split) && (a.dtype != KP_BF16 || a.res)) return cudaErrorInvalidValue;
+    if ((fb || split) && (a.dtype != KP_BF16 || a.res || a.M > 256)) return cudaErrorInvalidValue;
     if (a.dtype != KP_BF16 && a.dtype != KP_FP16) return cudaErrorInvalidValue;
     const int Mpad = mpad_of(a.M);
     const int nkb = nkb_of(c);
@@ -774,7 +785,8 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_attr_devices.count(dev)) {
-            for (auto fn : {tc05_kernel<false>, tc05_kernel<true>}) {
+            for (auto fn : {tc05_kernel<false, false>, tc05_kernel<true, false>,
+                            tc05_kernel<false, true>, tc05_kernel<true, true>}) {
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
                 if (e == cudaSuccess)
@@ -787,7 +799,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
 
     const int T = (a.N + kTileN - 1) / kTileN;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(T * p.C, 1, 1);
+    cfg.gridDim = dim3(T * p.C, (a.M + Mpad - 1) / Mpad, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     // TMEM is 512 columns per SM and an allocation that does not fit waits;
     // CTAs of a cluster wait for each other, so the CTAs that can share an SM
@@ -823,8 +835,10 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     cfg.attrs = attr;
     cfg.numAttrs = na;
     const bool general = a.dtype != KP_BF16 || a.res != nullptr;
-    return general ? cudaLaunchKernelEx(&cfg, tc05_kernel<true>, mw, mx, mx3, mfb, p)
-                   : cudaLaunchKernelEx(&cfg, tc05_kernel<false>, mw, mx, mx3, mfb, p);
+    const bool tiled = cfg.gridDim.y > 1;
+    auto fn = general ? (tiled ? tc05_kernel<true, true> : tc05_kernel<true, false>)
+                      : (tiled ? tc05_kernel<false, true> : tc05_kernel<false, false>);
+    return cudaLaunchKernelEx(&cfg, fn, mw, mx, mx3, mfb, p);
 }
 
 }  // namespace kp

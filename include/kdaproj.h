@@ -131,7 +131,9 @@ typedef struct kda_plan kda_plan;
  *   y   device, [M, N] bf16, row-major; written, never read
  *   cfg NULL or kind == KP_KIND_AUTO: the autotune table picks the kernel;
  *       otherwise the given configuration is validated and used.
- * M == 0 is a no-op. M > 256 is processed in 256-row slices.
+ * M == 0 is a no-op. The tcgen05 kernel takes any M in one launch: token
+ * tiles of up to 256 along the grid's second axis, which all read a weight
+ * tile while it is in L2 (the CUDA-core kernel takes M <= 16).
  * Scratch: split-K partial sums and tile counters live in a per-device
  * workspace owned by the library. It grows on demand, so the first call of a
  * larger shape may allocate (cudaMalloc); do one call per shape before stream

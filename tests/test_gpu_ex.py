@@ -81,7 +81,7 @@ def test_ex_kernels(dtype, residual, name, M):
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("M", [17, 64, 129, 256, 300])
 def test_ex_tc05_large_m(dtype, M):
-    # ragged N and a partial last K block; M = 300 runs as two 256-row slices
+    # ragged N and a partial last K block; M = 300 runs as two token tiles
     x, W, r = case(M, 264, 1032, dtype, seed=M)
     for C in (1, 4):
         check_ex(x, W, r, dtype, KpCfg.make("tc05", split_k=C, k_unroll=1), f"tc05 C={C}")

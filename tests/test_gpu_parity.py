@@ -119,7 +119,7 @@ def test_tc05_cluster_splits(C, nkb):
                    f"tc05 P={P}")
 
 
-def test_tc05_m_above_256_is_sliced():
+def test_tc05_m_above_256_two_token_tiles():
     x, W = gemm_case(300, 264, 512, seed=8)
     check_gemm(x, W, KpCfg.make("tc05", split_k=4, k_unroll=1), "tc05")
 
