@@ -57,15 +57,16 @@ def cc_candidates(M: int, N: int, K: int, sms: int):
 
 def tc05_candidates(M: int, N: int, K: int, sms: int):
     out = []
-    T = math.ceil(N / 128)
-    for C in (1, 2, 4, 8, 16):
-        if T * C > 2 * sms:
-            continue
-        for nkb in (1, 2, 4):
-            for P in sorted({1, min(nkb, 2), nkb}):
-                for stages in (0, 2, 3, 4):
-                    out.append(KpCfg.make("tc05", split_k=C, k_unroll=nkb, producers=P,
-                                          stages=stages))
+    for rows in (128, 256):   # feature rows per CTA (256: two accumulators share x)
+        T = math.ceil(N / rows)
+        for C in (1, 2, 4, 8, 16):
+            if T * C > 2 * sms:
+                continue
+            for nkb in (1, 2, 4):
+                for P in sorted({1, min(nkb, 2), nkb}):
+                    for stages in (0, 2, 3, 4):
+                        out.append(KpCfg.make("tc05", split_k=C, rows=rows, k_unroll=nkb,
+                                              producers=P, stages=stages))
     return out
 
 
@@ -148,12 +149,14 @@ def sweep_candidates(M: int, N: int, K: int, sms: int):
             for waves in (2, 4):
                 S = max(1, min(max(1, K // 256), round(waves * sms / tiles)))
                 out.append(KpCfg.make("cc", split_k=S, block=256, rows=R, k_unroll=U))
-    T = math.ceil(N / 128)
     KB = math.ceil(K / 64)
-    Cs = [C for C in (1, 2, 4, 8, 16) if C <= KB and T * C <= 2 * sms]
-    for C in sorted(Cs, reverse=True)[:2]:
-        for P in (1, 2):
-            out.append(KpCfg.make("tc05", split_k=C, k_unroll=2, producers=P, stages=0))
+    for rows in (128, 256) if M >= 32 else (128,):
+        T = math.ceil(N / rows)
+        Cs = [C for C in (1, 2, 4, 8, 16) if C <= KB and T * C <= 2 * sms]
+        for C in sorted(Cs, reverse=True)[:2]:
+            for P in (1, 2):
+                out.append(KpCfg.make("tc05", split_k=C, rows=rows, k_unroll=2 if M <= 128 else 1,
+                                      producers=P, stages=0))
     valid, seen = [], set()
     for c in out:
         key = tuple(getattr(c, f) for f, _ in c._fields_)
@@ -255,12 +258,13 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
         q_res = sweep_shape(M, pb.Nq, pb.K, sms, device, ("cc", "tc05"))[:top_q]
         b_res = sweep_shape(M, pb.Nfb, 128, sms, device, ("cc", "tc05", "smallk"))[:top_b]
         f_cands = []
-        for C in (1, 2, 4, 8, 16):
-            for nkb in (2, 4):
-                for stages in (2, 3):
-                    for fuse in (0, binding.FLAG_FUSE_FB):
-                        f_cands.append(KpCfg.make("tc05", split_k=C, k_unroll=nkb, stages=stages,
-                                                  flags=binding.FLAG_PDL | fuse))
+        for rows in (128, 256):
+            for C in (1, 2, 4, 8, 16):
+                for nkb in (1, 2, 4):
+                    for stages in (2, 3):
+                        for fuse in (0, binding.FLAG_FUSE_FB):
+                            f_cands.append(KpCfg.make("tc05", split_k=C, rows=rows, k_unroll=nkb,
+                                                      stages=stages, flags=binding.FLAG_PDL | fuse))
         if M <= 16:
             f_cands += [c for c in cc_candidates(M, pb.Nfab, pb.K, sms) if c.split_k <= 8]
         best = None

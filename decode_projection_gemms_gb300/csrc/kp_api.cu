@@ -219,7 +219,7 @@ static BranchShape branch_shape(const kda_plan *p, int b);
 // Q/K/V/G configuration c: tcgen05 kernel, F_A rows starting on a 128-row
 // tile, room for the fused F_B operands, no M slicing.
 static bool single_launch_ok(const kda_plan *p, int M, const kp_cfg &c) {
-    return c.kind == KP_KIND_TC05 && M <= 256 && p->Nq % 128 == 0 &&
+    return c.kind == KP_KIND_TC05 && M <= 256 && p->Nq % tc05_rows(c) == 0 &&
            tc05_supported(M, p->Nq + p->Nfab, p->K, c) && tc05_fusable(M, c);
 }
 
@@ -606,7 +606,7 @@ int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, cons
         fb.N = g.N;
         fb.y = g.y;
         fb.ld = g.ldy;
-        fb.tile = plan->Nq / 128;
+        fb.row0 = plan->Nq;
         kp_cfg c = cq;
         c.flags &= ~KP_FLAG_FUSE_FB;
         if ((e = tc05_launch(a, c, plan->sms, ms, &fb, &so)) != cudaSuccess)
@@ -626,7 +626,7 @@ int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, cons
             fb.N = g.N;
             fb.y = g.y;
             fb.ld = g.ldy;
-            fb.tile = 0;
+            fb.row0 = 0;
             return tc05_launch(f, c, plan->sms, st, &fb);
         }
         cudaError_t e2 = launch_gemm(f, c, plan->sms, st);

@@ -43,14 +43,15 @@ bool cc_supported(int M, int K, const kp_cfg &c);
 Scratch cc_scratch(int M, int N, int K, const kp_cfg &c);
 cudaError_t cc_launch(const GemmArgs &a, const kp_cfg &c, cudaStream_t s);
 
-// F_B fused into the F_A/beta launch: tile `tile` of that GEMM holds the 128
-// F_A rows; y = bf16(bf16(F_A) * W^T) with W [N, 128].
+// F_B fused into the F_A/beta launch: rows [row0, row0 + 128) of that GEMM are
+// F_A (row0 a multiple of the configuration's rows per CTA);
+// y = bf16(bf16(F_A) * W^T) with W [N, 128].
 struct FusedFB {
     const __nv_bfloat16 *W;
     int N;
     __nv_bfloat16 *y;
     int64_t ld;
-    int tile;
+    int row0;
 };
 
 // Rows n >= n_split of a GEMM's output go to a second matrix y2 (row
@@ -68,6 +69,7 @@ Scratch tc05_scratch(int M, int N, int K, const kp_cfg &c, int num_sms);
 cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStream_t s,
                         const FusedFB *fb = nullptr, const SplitOut *split = nullptr);
 int tc05_max_stages(int M);
+int tc05_rows(const kp_cfg &c);   // feature rows per CTA of a configuration (128 or 256)
 kp_cfg tc05_default(int M, int N, int K, int num_sms);
 
 // small-K kernel (kp_smallk.cu)

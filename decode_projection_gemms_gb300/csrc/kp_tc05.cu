@@ -144,7 +144,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // true: the element type and the residual come from the parameters.
 // kTiled = false: one token tile (M <= 256); true: token tiles along the
 // grid's y axis.
-template <bool kGeneral, bool kTiled>
+// kWide = false: a CTA owns 128 feature rows; true: 256, as two 128-row MMAs
+// on the same x operand into two TMEM accumulators (x per weight byte halves).
+template <bool kGeneral, bool kTiled, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
     tc05_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                 const __grid_constant__ CUtensorMap tmx3, const __grid_constant__ CUtensorMap tmfb,
@@ -187,7 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pidx = (warp == 0) ? 0 : (warp >= 2 && warp - 1 < p.producers) ? warp - 1 : -1;
     const int P = p.producers;
     const uint32_t xblk = static_cast<uint32_t>(p.Mpad) * kBlockK * 2;
-    const int row0 = tile * kTileN;
+    constexpr int RT = kWide ? 2 * kTileN : kTileN;               // feature rows per CTA
+    constexpr uint32_t kWBlk = static_cast<uint32_t>(RT) * kBlockK * 2;  // W bytes per K block
+    const int row0 = tile * RT;
     const int pre = n_st < S ? n_st : S;
     // W boxes of stage s of this CTA's range, producer pidx's share; producer
     // 0 also accounts for the stage's x bytes.
@@ -198,11 +202,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bar = smem_u32(full + stage);
         int mine = 0;
         for (int j = pidx; j < kbs; j += P) ++mine;
-        uint32_t bytes = static_cast<uint32_t>(mine) * kWBlockBytes;
+        uint32_t bytes = static_cast<uint32_t>(mine) * kWBlk;
         if (pidx == 0) bytes += static_cast<uint32_t>(kbs) * xblk;
         mbar_expect_tx(bar, bytes);   // every producer arrives once per stage
         for (int j = pidx; j < kbs; j += P)
-            tma_load_2d(st + j * kWBlockBytes, &tmw, bar, (k0 + j) * kBlockK, row0, pol_w);
+            for (int h = 0; h < RT / kTileN; ++h)   // 128-row boxes
+                tma_load_2d(st + j * kWBlk + h * kWBlockBytes, &tmw, bar, (k0 + j) * kBlockK,
+                            row0 + h * kTileN, pol_w);
     };
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) {
@@ -314,13 +320,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t st = base + stage * p.stage_bytes;
                 for (int j = 0; j < kbs; ++j) {
-                    const uint64_t ad = smem_desc(st + j * kWBlockBytes, 1024);
+                    const uint64_t ad = smem_desc(st + j * kWBlk, 1024);
                     const uint64_t bd = smem_desc(st + p.w_stage_bytes + j * xblk, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kBlockK / 16; ++kk)
                         // +32 bytes per 16-element K step inside the swizzle atom
                         umma_bf16(tmem_base, ad + 2 * kk, bd + 2 * kk, p.idesc,
                                   (s > 0 || j > 0 || kk > 0) ? 1u : 0u);
+                    if constexpr (kWide) {
+                        // rows 128..255 of the box (16 KB on), same x, next accumulator
+                        const uint64_t ad1 = smem_desc(st + j * kWBlk + kWBlockBytes, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < kBlockK / 16; ++kk)
+                            umma_bf16(tmem_base + static_cast<uint32_t>(p.Mpad), ad1 + 2 * kk, bd + 2 * kk,
+                                      p.idesc, (s > 0 || j > 0 || kk > 0) ? 1u : 0u);
+                    }
                 }
                 umma_commit(smem_u32(empty + stage));
             }
@@ -329,16 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
         const int q = warp & 3;          // TMEM lane quarter this warp may read
-        const int row = q * 32 + lane;   // feature row within the tile
-        const int n = tile * kTileN + row;
+        const int row = q * 32 + lane;   // feature row within a 128-row half of the tile
         __syncwarp();   // lane 0 may have been producing
         pdl_wait();
         if constexpr (kGeneral) {
             if (p.res) {
                 // Pull the residual this CTA adds at the end (its rows of the
                 // tile, every token) into L2 while the main loop runs.
-                const int rows = C == 1 ? kTileN : kTileN / C;
-                const int nr0 = tile * kTileN + (C == 1 ? 0 : rank * rows);
+                const int rows = C == 1 ? RT : RT / C;
+                const int nr0 = tile * RT + (C == 1 ? 0 : rank * rows);
                 const int segs = (rows + 31) / 32;   // 64-byte pieces per token
                 for (int i = threadIdx.x - 64; i < Mloc * segs; i += kThreads - 64) {
                     const int m = i / segs;
@@ -351,29 +364,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(smem_u32(accf), 0, abort_flag, p.err, DEV_TIMEOUT_ACC_FULL);
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        float *red = reinterpret_cast<float *>(gbase);  // [Mpad][128] fp32, reuses stage memory
-        auto take = [&](int m, float f) {
-            if (C == 1) {
-                uint16_t b;
-                if constexpr (kGeneral) {
-                    b = n < p.N ? finish(p, m0 + m, n, f) : 0;
+        float *red = reinterpret_cast<float *>(gbase);  // [Mpad][RT] fp32, reuses stage memory
+        // half h of the tile: rows h*128 .. h*128+127, accumulator columns h*Mpad ..
+        for (int h = 0; h < (kWide ? 2 : 1); ++h) {
+            const int rt = h * kTileN + row;   // row within the tile
+            const int n = tile * RT + rt;
+            auto take = [&](int m, float f) {
+                if (C == 1) {
+                    uint16_t b;
+                    if constexpr (kGeneral) {
+                        b = n < p.N ? finish(p, m0 + m, n, f) : 0;
+                    } else {
+                        b = bf16_bits_rn(f);
+                        if (n < p.N) store_bits(p, m0 + m, n, b);
+                    }
+                    if (fused && h == 0)   // F_A = the fused tile's first 128 rows
+                        *reinterpret_cast<uint16_t *>(gbase + p.off_bfa + bfa_offset(m, row, p.Mpad)) = b;
                 } else {
-                    b = bf16_bits_rn(f);
-                    if (n < p.N) store_bits(p, m0 + m, n, b);
+                    red[m * RT + rt] = f;
                 }
-                if (fused)
-                    *reinterpret_cast<uint16_t *>(gbase + p.off_bfa + bfa_offset(m, row, p.Mpad)) = b;
-            } else {
-                red[m * kTileN + row] = f;
-            }
-        };
-        for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
-            uint32_t va[16];
-            tmem_ld16(taddr + c0, va);
-            tmem_ld_wait();
+            };
+            const uint32_t tcol = taddr + static_cast<uint32_t>(h * p.Mpad);
+            for (int c0 = 0; c0 < p.Mpad; c0 += 16) {
+                uint32_t va[16];
+                tmem_ld16(tcol + c0, va);
+                tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (c0 + i < Mloc) take(c0 + i, __uint_as_float(va[i]));
+                for (int i = 0; i < 16; ++i)
+                    if (c0 + i < Mloc) take(c0 + i, __uint_as_float(va[i]));
+            }
         }
         tc_fence_before();
     }
@@ -382,14 +401,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // All partial tiles of the cluster are in shared memory after this.
         __syncwarp();
         cluster_sync_all();
-        const int rpc = kTileN / C;             // rows reduced by this CTA (>= 8)
+        const int rpc = RT / C;                 // rows reduced by this CTA (>= 8)
         const int groups = rpc / 4;             // float4 groups per token
         const int r0 = rank * rpc;
         const uint32_t red_base = base;         // same offset in every CTA
         for (int idx = threadIdx.x; idx < Mloc * groups; idx += kThreads) {
             const int m = idx / groups;
             const int rr = r0 + 4 * (idx - m * groups);
-            const uint32_t off = red_base + static_cast<uint32_t>((m * kTileN + rr) * 4);
+            const uint32_t off = red_base + static_cast<uint32_t>((m * RT + rr) * 4);
             float4 part[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c)
@@ -403,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc.z += part[c].z;
                     acc.w += part[c].w;
                 }
-            const int nb = tile * kTileN + rr;
+            const int nb = tile * RT + rr;
             uint32_t b0, b1, b2, b3;
             if constexpr (kGeneral) {
                 b0 = nb + 0 < p.N ? finish(p, m0 + m, nb + 0, acc.x) : 0;
@@ -420,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nb + 2 < p.N) store_bits(p, m0 + m, nb + 2, b2);
                 if (nb + 3 < p.N) store_bits(p, m0 + m, nb + 3, b3);
             }
-            if (fused) {
+            if (fused && rr < kTileN) {
                 // this rank's features rr..rr+3 of the F_B operand (8 bytes),
                 // written into its own copy and into every CTA of the cluster
                 // that computes F_B tiles (the F_B operand region lies past
@@ -597,14 +616,18 @@ cudaError_t make_map3(CUtensorMap *map, const void *ptr, int rows, int cols, int
 // Tokens per CTA (the MMA's N): M padded to 16, at most 256 (one token tile).
 int mpad_of(int M) { return ((M < 256 ? M : 256) + 15) & ~15; }
 
-uint32_t w_stage_bytes_of(int nkb) { return static_cast<uint32_t>(nkb) * kWBlockBytes; }
+// Feature rows per CTA: 256 when the configuration asks for it (rows = 256),
+// else 128.
+int rows_of(const kp_cfg &c) { return c.rows == 2 * kTileN ? 2 * kTileN : kTileN; }
 
-uint32_t stage_bytes_of(int Mpad, int nkb) {
-    return w_stage_bytes_of(nkb) + static_cast<uint32_t>(nkb) * Mpad * kBlockK * 2;
+uint32_t w_stage_bytes_of(int nkb, int rt) { return static_cast<uint32_t>(nkb) * rt * kBlockK * 2; }
+
+uint32_t stage_bytes_of(int Mpad, int nkb, int rt) {
+    return w_stage_bytes_of(nkb, rt) + static_cast<uint32_t>(nkb) * Mpad * kBlockK * 2;
 }
 
-size_t smem_of(int Mpad, int nkb, int stages) {
-    return static_cast<size_t>(stages) * stage_bytes_of(Mpad, nkb) + 1024 + kBarBytes;
+size_t smem_of(int Mpad, int nkb, int stages, int rt) {
+    return static_cast<size_t>(stages) * stage_bytes_of(Mpad, nkb, rt) + 1024 + kBarBytes;
 }
 
 uint32_t tmem_cols_of(int Mpad) {
@@ -613,8 +636,8 @@ uint32_t tmem_cols_of(int Mpad) {
     return c;
 }
 
-int max_stages(int Mpad, int nkb) {
-    int s = static_cast<int>((kMaxSmem - 1024 - kBarBytes) / stage_bytes_of(Mpad, nkb));
+int max_stages(int Mpad, int nkb, int rt) {
+    int s = static_cast<int>((kMaxSmem - 1024 - kBarBytes) / stage_bytes_of(Mpad, nkb, rt));
     return s > 16 ? 16 : s;
 }
 
@@ -624,7 +647,7 @@ int nkb_of(const kp_cfg &c) { return c.k_unroll < 1 ? 1 : c.k_unroll; }
 
 }  // namespace
 
-int tc05_max_stages(int M) { return max_stages(mpad_of(M), 1); }
+int tc05_max_stages(int M) { return max_stages(mpad_of(M), 1, kTileN); }
 
 kp_cfg tc05_default(int M, int N, int K, int num_sms) {
     kp_cfg c = {};
@@ -637,11 +660,25 @@ kp_cfg tc05_default(int M, int N, int K, int num_sms) {
     while (C < 16 && T * mt * C * 2 <= num_sms && C * 2 <= KB) C *= 2;
     const int Mpad = mpad_of(M);
     int nkb = 4;
-    while (nkb > 1 && max_stages(Mpad, nkb) < 3) nkb /= 2;
+    while (nkb > 1 && max_stages(Mpad, nkb, kTileN) < 3) nkb /= 2;
     c.split_k = C;
     c.k_unroll = nkb;
     c.producers = nkb;
     c.stages = 0;
+    if (mt > 1) {
+        // Prefill (measured on N=4096, K=7168): while the 128-row grid fits
+        // on the SMs, deep stages of two K blocks (M=1024: 877 TFLOP/s);
+        // beyond that, 256-row CTAs that share each x tile between two
+        // accumulators (M=4096: 1125 TFLOP/s; 128 rows, max stages: 781).
+        c.split_k = 1;
+        c.producers = 1;
+        if (T * mt <= num_sms) {
+            c.k_unroll = 2;
+        } else {
+            c.rows = 2 * kTileN;
+            c.k_unroll = 1;
+        }
+    }
     return c;
 }
 
@@ -656,11 +693,12 @@ bool tc05_supported(int M, int N, int K, const kp_cfg &c) {
     if (nkb != 1 && nkb != 2 && nkb != 4) return false;
     if (c.producers < 0 || c.producers > 5) return false;
     const int Mpad = mpad_of(M);
-    const int ms = max_stages(Mpad, nkb);
+    const int rt = rows_of(c);
+    const int ms = max_stages(Mpad, nkb, rt);
     const int st = c.stages ? c.stages : ms;
     if (st < 1 || st > ms) return false;
-    // the cluster reduction reuses the stage memory for an Mpad x 128 fp32 tile
-    if (C > 1 && static_cast<size_t>(Mpad) * kTileN * 4 > static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb))
+    // the cluster reduction reuses the stage memory for an Mpad x rows fp32 tile
+    if (C > 1 && static_cast<size_t>(Mpad) * rt * 4 > static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb, rt))
         return false;
     return true;
 }
@@ -669,11 +707,11 @@ Scratch tc05_scratch(int, int, int, const kp_cfg &, int) { return Scratch(); }
 
 namespace {
 // Shared-memory layout of the fused F_B after the main loop (offsets from the
-// 1024-aligned base): [partial tile Mpad x 128 fp32][F_A operand 2 x Mpad x
+// 1024-aligned base): [partial tile Mpad x rt fp32][F_A operand 2 x Mpad x
 // 128 B][nbuf W_fb tiles of 2 x 16 KB]. It must fit in the pipeline memory.
-void fb_layout(int Mpad, uint32_t *off_bfa, uint32_t *off_wfb, uint32_t *end, int nbuf = 1) {
+void fb_layout(int Mpad, int rt, uint32_t *off_bfa, uint32_t *off_wfb, uint32_t *end, int nbuf = 1) {
     auto al = [](uint32_t v) { return (v + 1023u) & ~1023u; };
-    *off_bfa = al(static_cast<uint32_t>(Mpad) * kTileN * 4);
+    *off_bfa = al(static_cast<uint32_t>(Mpad) * rt * 4);
     *off_wfb = al(*off_bfa + static_cast<uint32_t>(Mpad) * 256);
     *end = *off_wfb + static_cast<uint32_t>(nbuf) * 2 * kWBlockBytes;
 }
@@ -683,11 +721,14 @@ bool tc05_fusable(int M, const kp_cfg &c) {
     if (M < 1 || M > 256) return false;
     const int Mpad = mpad_of(M);
     const int nkb = nkb_of(c);
-    const int st = c.stages ? c.stages : max_stages(Mpad, nkb);
+    const int rt = rows_of(c);
+    const int st = c.stages ? c.stages : max_stages(Mpad, nkb, rt);
     uint32_t ob, ow, end;
-    fb_layout(Mpad, &ob, &ow, &end);
-    return end <= static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb);
+    fb_layout(Mpad, rt, &ob, &ow, &end);
+    return end <= static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb, rt);
 }
+
+int tc05_rows(const kp_cfg &c) { return rows_of(c); }
 
 cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStream_t stream,
                         const FusedFB *fb, const SplitOut *split) {
@@ -699,7 +740,8 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     if (a.dtype != KP_BF16 && a.dtype != KP_FP16) return cudaErrorInvalidValue;
     const int Mpad = mpad_of(a.M);
     const int nkb = nkb_of(c);
-    const int stages = c.stages ? c.stages : max_stages(Mpad, nkb);
+    const int rt = rows_of(c);
+    const int stages = c.stages ? c.stages : max_stages(Mpad, nkb, rt);
     Tc05Params p;
     p.y = a.y;
     p.ldy = a.ldy;
@@ -707,7 +749,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.y2 = nullptr;
     p.ldy2 = 0;
     if (split) {
-        if (split->n_split % kTileN) return cudaErrorInvalidValue;
+        if (split->n_split % rt) return cudaErrorInvalidValue;
         p.n_split = split->n_split;
         p.y2 = split->y2;
         p.ldy2 = split->ldy2;
@@ -724,7 +766,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.nkb = nkb;
     p.producers = producers_of(c);
     p.stages = stages;
-    p.n_tiles = (a.N + kTileN - 1) / kTileN;
+    p.n_tiles = (a.N + rt - 1) / rt;
     p.tile_rot = 0;
     // kind::f16 instruction descriptor: D fp32 (bit 4), A and B formats at
     // bits 7 and 10 (1 = bf16, 0 = fp16), both K-major, N >> 3 at bit 17,
@@ -732,9 +774,9 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     const uint32_t ab = a.dtype == KP_FP16 ? 0u : (1u << 7) | (1u << 10);
     p.idesc = (1u << 4) | ab | (static_cast<uint32_t>(Mpad >> 3) << 17) |
               (static_cast<uint32_t>(kTileN >> 4) << 24);
-    p.tmem_cols = tmem_cols_of(Mpad);
-    p.stage_bytes = stage_bytes_of(Mpad, nkb);
-    p.w_stage_bytes = w_stage_bytes_of(nkb);
+    p.tmem_cols = tmem_cols_of(rt / kTileN * Mpad);   // one accumulator per 128-row half
+    p.stage_bytes = stage_bytes_of(Mpad, nkb, rt);
+    p.w_stage_bytes = w_stage_bytes_of(nkb, rt);
     p.fb_tile = -1;
     p.fb_tiles = 0;
     p.N_fb = 0;
@@ -748,19 +790,21 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     memset(&mfb, 0, sizeof mfb);
     if (fb) {
         uint32_t end;
-        fb_layout(Mpad, &p.off_bfa, &p.off_wfb, &end);
+        fb_layout(Mpad, rt, &p.off_bfa, &p.off_wfb, &end);
+        if (fb->row0 % rt) return cudaErrorInvalidValue;   // F_A rows start a tile
         // a buffer per F_B tile of a CTA when they fit (else one, refilled),
         // and two TMEM accumulators when a CTA has several tiles
         const int tiles = (fb->N + kTileN - 1) / kTileN;
         const int per_cta = (tiles + p.C - 1) / p.C;
-        const size_t pipe = static_cast<size_t>(stages) * stage_bytes_of(Mpad, nkb);
+        const size_t pipe = static_cast<size_t>(stages) * stage_bytes_of(Mpad, nkb, rt);
         uint32_t ob, ow, end_all;
-        fb_layout(Mpad, &ob, &ow, &end_all, per_cta);
+        fb_layout(Mpad, rt, &ob, &ow, &end_all, per_cta);
         p.fb_bufs = (per_cta <= kMaxFbBufs && end_all <= pipe) ? per_cta : 1;
         p.fb_accs = (p.fb_bufs >= per_cta && per_cta > 1 && 2 * Mpad <= 256) ? 2 : 1;
         p.tmem_cols_fb = tmem_cols_of(p.fb_accs * Mpad);
-        p.fb_tile = fb->tile;
-        p.tile_rot = fb->tile;
+        if (p.tmem_cols_fb < p.tmem_cols) p.tmem_cols_fb = p.tmem_cols;
+        p.fb_tile = fb->row0 / rt;
+        p.tile_rot = p.fb_tile;
         p.N_fb = fb->N;
         p.fb_tiles = (fb->N + kTileN - 1) / kTileN;
         p.yfb = fb->y;
@@ -785,8 +829,10 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_attr_devices.count(dev)) {
-            for (auto fn : {tc05_kernel<false, false>, tc05_kernel<true, false>,
-                            tc05_kernel<false, true>, tc05_kernel<true, true>}) {
+            for (auto fn : {tc05_kernel<false, false, false>, tc05_kernel<true, false, false>,
+                            tc05_kernel<false, true, false>, tc05_kernel<true, true, false>,
+                            tc05_kernel<false, false, true>, tc05_kernel<true, false, true>,
+                            tc05_kernel<false, true, true>, tc05_kernel<true, true, true>}) {
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
                 if (e == cudaSuccess)
@@ -797,7 +843,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
         }
     }
 
-    const int T = (a.N + kTileN - 1) / kTileN;
+    const int T = (a.N + rt - 1) / rt;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(T * p.C, (a.M + Mpad - 1) / Mpad, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -806,7 +852,7 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     // must never need more than 512 columns together. Shared memory bounds
     // what shares an SM: each CTA takes at least cols/512 of the SM's shared
     // memory (with its per-block reserve), so any mix of such CTAs fits.
-    size_t smem = smem_of(Mpad, nkb, stages);
+    size_t smem = smem_of(Mpad, nkb, stages, rt);
     {
         const uint32_t cols = p.tmem_cols_fb > p.tmem_cols ? p.tmem_cols_fb : p.tmem_cols;
         int sm_smem = 0, reserved = 0;
@@ -836,8 +882,13 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     cfg.numAttrs = na;
     const bool general = a.dtype != KP_BF16 || a.res != nullptr;
     const bool tiled = cfg.gridDim.y > 1;
-    auto fn = general ? (tiled ? tc05_kernel<true, true> : tc05_kernel<true, false>)
-                      : (tiled ? tc05_kernel<false, true> : tc05_kernel<false, false>);
+    using Fn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Tc05Params);
+    static const Fn kernels[2][2][2] = {
+        {{tc05_kernel<false, false, false>, tc05_kernel<false, false, true>},
+         {tc05_kernel<false, true, false>, tc05_kernel<false, true, true>}},
+        {{tc05_kernel<true, false, false>, tc05_kernel<true, false, true>},
+         {tc05_kernel<true, true, false>, tc05_kernel<true, true, true>}}};
+    const Fn fn = kernels[general][tiled][rt == 2 * kTileN];
     return cudaLaunchKernelEx(&cfg, fn, mw, mx, mx3, mfb, p);
 }
 

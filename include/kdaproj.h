@@ -113,7 +113,9 @@ typedef struct kp_cfg {
     int32_t block;    /* CC, SMALLK: threads per CTA (multiple of 32; CC <= 256,
                          SMALLK <= 256) */
     int32_t rows;     /* CC: output rows per warp (1, 2, 4, 8);
-                         SMALLK: output rows per CTA (1..64) */
+                         SMALLK: output rows per CTA (1..64);
+                         TC05: feature rows per CTA, 256 (two 128-row MMAs
+                         sharing each x tile) or anything else for 128 */
     int32_t k_unroll; /* CC: 16-byte W loads in flight per row per lane (1, 2, 4);
                          TC05: 64-wide K blocks per pipeline stage (1, 2, 4) */
     int32_t producers;/* TC05: warps issuing TMA copies per CTA (1..5; 0 = 1) */

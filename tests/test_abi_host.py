@@ -84,6 +84,11 @@ def test_builtin_rule(lib):
         assert c.kind == binding.KIND_TC05
         c = binding.select_config(8, 1024, 128, num_sms=152)
         assert c.kind == binding.KIND_SMALLK
+        # prefill: one launch, no split-K; 256-row CTAs once 128-row ones outnumber the SMs
+        c = binding.select_config(1024, 4096, 7168, num_sms=152)
+        assert (c.kind, c.split_k, c.rows, c.k_unroll) == (binding.KIND_TC05, 1, 0, 2)
+        c = binding.select_config(4096, 4096, 7168, num_sms=152)
+        assert (c.kind, c.split_k, c.rows, c.k_unroll) == (binding.KIND_TC05, 1, 256, 1)
     finally:
         binding.table_load()
 
@@ -143,6 +148,12 @@ def test_scratch_sizes(lib):
                    binding.KpCfg.make("tc05", producers=6)):
         with pytest.raises(binding.KdaProjError):
             binding.scratch_bytes(20, 4096, 7168, bad_tc, 152)
+    # 256 feature rows per CTA: the cluster reduction needs Mpad x 256 fp32
+    wide = binding.KpCfg.make("tc05", split_k=4, rows=256, k_unroll=1)
+    assert binding.scratch_bytes(64, 4096, 7168, wide, 152) == 0
+    with pytest.raises(binding.KdaProjError):
+        binding.scratch_bytes(256, 4096, 7168, binding.KpCfg.make("tc05", split_k=4, rows=256,
+                                                                  k_unroll=2), 152)
     bad = binding.KpCfg.make("cc", split_k=1, block=256, rows=8, k_unroll=1)
     with pytest.raises(binding.KdaProjError) as e:
         binding.scratch_bytes(16, 4096, 7168, bad, 152)     # 8 x 16 accumulators: not built

@@ -88,6 +88,18 @@ def test_prefill_residual(dtype):
         sampled_check(y, bits16(x), bits16(W), f"{dtype} residual", dtype=dtype, res_bits=bits16(r))
 
 
+def test_prefill_default_large_grid():
+    # more 128-row CTAs than SMs: the built-in rule switches to 256-row CTAs
+    M, N, K = 2560, 4096, 1024
+    cfg = binding.select_config(M, N, K, 152)
+    x = gen_x(M, K, seed=21)
+    W = gen_w(N, K, seed=22)
+    y = poisoned((M, N))
+    binding.skinny_gemm(x.cuda(), W.cuda(), y)
+    torch.cuda.synchronize()
+    sampled_check(y, bf16_bits(x), bf16_bits(W), f"default {cfg.as_dict()}", seed=3)
+
+
 def test_prefill_closed_form():
     # all ones over 2048 tokens in 8 token tiles: every output is K exactly
     M, N, K = 2048, 136, 7168
