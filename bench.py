@@ -272,8 +272,8 @@ def run_ours(args):
         tot_one, _ = timed(graphs_one, args.cmp_steps)
         tot_q, _ = timed(graphs_q, args.cmp_steps)
     e2e = run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist)
-    ex = run_ex(args, wp_stack, dev, main, hbm_peak, dist)
-    prefill = run_prefill(args, wp_stack, dev, main, tc_peak_burst, dist)
+    ex = None if args.no_extras else run_ex(args, wp_stack, dev, main, hbm_peak, dist)
+    prefill = None if args.no_extras else run_prefill(args, wp_stack, dev, main, tc_peak_burst, dist)
     clock_info = clocks.stop()
 
     # reductions (max over ranks)
@@ -604,6 +604,8 @@ def main():
     ap.add_argument("--cpu-stride", type=int, default=16,
                     help="column sampling stride of the CPU oracle")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the skinny_gemm_ex and prefill measurements (e.g. for profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
