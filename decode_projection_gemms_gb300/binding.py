@@ -37,7 +37,9 @@ EXPORTS = (
     "kda_proj_plan", "kda_proj_set_overlap", "kda_proj_get_config", "kda_proj_set_config",
     "kda_proj_overlap_at", "kda_proj_run", "kda_proj_destroy", "kp_last_error", "kp_version",
     "kp_device_error", "kp_scratch_bytes", "skinny_gemm_noalloc", "skinny_gemm_ex",
+    "kp_selftest_timeout",
 )
+DEV_SELFTEST = 5   # device error code of kp_selftest_timeout
 
 
 class KdaProjError(RuntimeError):
@@ -99,6 +101,7 @@ def load(path: str | None = None):
             "kp_scratch_bytes": [ci, ci, ci, cfgp, ci, ctypes.POINTER(ctypes.c_size_t)],
             "skinny_gemm_noalloc": [vp, vp, vp, ci, ci, ci, cfgp, vp],
             "skinny_gemm_ex": [vp, vp, vp, vp, ci, ci, ci, ci, cfgp, vp],
+            "kp_selftest_timeout": [ci, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -160,6 +163,11 @@ def scratch_bytes(M: int, N: int, K: int, cfg: KpCfg, num_sms: int) -> int:
     b = ctypes.c_size_t()
     _check(load().kp_scratch_bytes(M, N, K, ctypes.byref(cfg), num_sms, ctypes.byref(b)))
     return int(b.value)
+
+
+def selftest_timeout(timeout_us: int = 2000, stream=None):
+    """Launch the failure-path self-test (a wait that must run out)."""
+    _check(load().kp_selftest_timeout(int(timeout_us), _stream_handle(stream)))
 
 
 def device_error() -> int:

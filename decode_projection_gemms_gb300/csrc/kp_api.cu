@@ -330,6 +330,34 @@ int kp_scratch_bytes(int M, int N, int K, const kp_cfg *cfg, int num_sms, size_t
     return KP_OK;
 }
 
+// One CTA waits on a barrier that nothing completes; the bounded wait must
+// give up after limit_ns, record DEV_SELFTEST and let the kernel exit.
+__global__ void selftest_timeout_kernel(int *err, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_wait_bounded(smem_u32(&bar), 0, &abort_flag, err, DEV_SELFTEST, limit_ns);
+}
+
+int kp_selftest_timeout(int timeout_us, kp_stream_t stream) {
+    if (timeout_us < 1 || timeout_us > 1000000)
+        return set_error(KP_EINVAL, "kp_selftest_timeout: timeout_us=%d outside 1..1000000", timeout_us);
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    selftest_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        d->err, static_cast<unsigned long long>(timeout_us) * 1000ull);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kp_selftest_timeout launch");
+    return KP_OK;
+}
+
 int kp_device_error(int *code) {
     if (!code) return set_error(KP_EINVAL, "kp_device_error: NULL");
     DevState *d = nullptr;

@@ -85,7 +85,8 @@ enum DevErr {
     DEV_TIMEOUT_FULL = 1,     // MMA warp waited too long for a TMA stage
     DEV_TIMEOUT_EMPTY = 2,    // producer waited too long for a free stage
     DEV_TIMEOUT_ACC_FULL = 3, // epilogue waited too long for an accumulator
-    DEV_TIMEOUT_ACC_EMPTY = 4 // MMA warp waited too long for a free accumulator
+    DEV_TIMEOUT_ACC_EMPTY = 4, // MMA warp waited too long for a free accumulator
+    DEV_SELFTEST = 5           // kp_selftest_timeout's wait ran out (as it must)
 };
 
 }  // namespace kp
@@ -193,20 +194,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Bounded wait: spins on the barrier phase; after ~1 s of wall time (or once
-// another wait in this CTA has given up) it records `code` in the error word,
-// raises the CTA's abort flag and returns false. The caller then proceeds as
-// if the phase had completed: every address it touches stays in bounds, so a
-// broken pipeline yields wrong numbers and an error code, never a hang.
+// Bounded wait: spins on the barrier phase; after `limit_ns` of wall time
+// (~1 s by default; or once another wait in this CTA has given up) it records
+// `code` in the error word, raises the CTA's abort flag and returns false. The
+// caller then proceeds as if the phase had completed: every address it touches
+// stays in bounds, so a broken pipeline yields wrong numbers and an error
+// code, never a hang.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int *abort_flag, int *err,
-                                                  int code) {
+                                                  int code, uint64_t limit_ns = 1000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > 1000000000ull) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
             if (err) atomicCAS(err, 0, code);
             return false;

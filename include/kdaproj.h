@@ -279,9 +279,18 @@ KP_API int kda_proj_destroy(kda_plan *plan);
 KP_API const char *kp_last_error(void);           /* thread-local, never NULL */
 KP_API int kp_version(void);                       /* KDAPROJ_VERSION */
 /* Reads and clears the device-side error word of the current device: 0 if
- * no kernel wait has run out, else the code of the first one (synchronous:
- * it waits for the device). Returns KP_OK or KP_ECUDA. */
+ * no kernel wait has run out, else the code of the first one: 1 a stage of
+ * operands never landed, 2 a pipeline stage was never freed, 3 an
+ * accumulator was never ready, 4 an accumulator was never drained, 5 the
+ * self-test below (synchronous: it waits for the device).
+ * Returns KP_OK or KP_ECUDA. */
 KP_API int kp_device_error(int *code);
+/* Self-test of the failure path: launches one CTA on `stream` that waits on a
+ * barrier nothing completes, with the kernels' bounded wait cut to timeout_us
+ * (1 .. 1000000). The wait gives up, records code 5 in the device error word
+ * and the kernel exits; the context stays usable. Not part of the
+ * projections. Returns KP_OK, KP_EINVAL, KP_ENODEV or KP_ECUDA. */
+KP_API int kp_selftest_timeout(int timeout_us, kp_stream_t stream);
 /* Bytes of scratch a configuration needs for (M, N, K), for tests/tools. */
 KP_API int kp_scratch_bytes(int M, int N, int K, const kp_cfg *cfg, int num_sms, size_t *bytes);
 
