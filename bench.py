@@ -464,31 +464,61 @@ def run_prefill(args, wp_stack, dev, main, tc_peak, dist, m_pre=(256, 1024, 4096
 
 def run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist):
     """Same metric through the public API with host buffers: every call copies
-    its x from pinned host memory and its three outputs back."""
+    its x from pinned host memory and its three outputs back. The copies run
+    on two side streams with double-buffered device buffers, so call i's
+    outputs go back and call i+1's x comes in while the device computes."""
     import torch
     from decode_projection_gemms_gb300.inputs import gen_x
     L = args.layers
+    cin = torch.cuda.Stream(device=dev)
+    cout = torch.cuda.Stream(device=dev)
     hx = {M: gen_x(M, K, seed=M).pin_memory() for M in m_list}
-    dx = {M: torch.empty((M, K), dtype=torch.bfloat16, device=dev) for M in m_list}
-    dout = {M: (torch.empty((M, N_QKVG), dtype=torch.bfloat16, device=dev),
-                torch.empty((M, N_FAB), dtype=torch.bfloat16, device=dev),
-                torch.empty((M, N_FB), dtype=torch.bfloat16, device=dev)) for M in m_list}
-    hout = {M: tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dout[M])
+    dx = {M: [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+          for M in m_list}
+    dout = {M: [(torch.empty((M, N_QKVG), dtype=torch.bfloat16, device=dev),
+                 torch.empty((M, N_FAB), dtype=torch.bfloat16, device=dev),
+                 torch.empty((M, N_FB), dtype=torch.bfloat16, device=dev)) for _ in range(2)]
             for M in m_list}
+    hout = {M: tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dout[M][0])
+            for M in m_list}
+
+    def calls(M):
+        ev_in = [torch.cuda.Event() for _ in range(L)]
+        ev_run = [torch.cuda.Event() for _ in range(L)]
+        ev_out = [torch.cuda.Event() for _ in range(L)]
+        start = torch.cuda.Event()
+        start.record(main)
+        cin.wait_event(start)
+        cout.wait_event(start)
+        for layer in range(L):
+            b = layer % 2
+            with torch.cuda.stream(cin):
+                if layer >= 2:
+                    cin.wait_event(ev_run[layer - 2])     # dx[b] is free again
+                dx[M][b].copy_(hx[M], non_blocking=True)
+                ev_in[layer].record(cin)
+            main.wait_event(ev_in[layer])
+            if layer >= 2:
+                main.wait_event(ev_out[layer - 2])        # dout[b] has been read back
+            plan.run(dx[M][b], wp_stack[layer], wfb_stack[layer], *dout[M][b],
+                     aux_stream=aux, events=evs)
+            ev_run[layer].record(main)
+            with torch.cuda.stream(cout):
+                cout.wait_event(ev_run[layer])
+                for d, h in zip(dout[M][b], hout[M]):
+                    h.copy_(d, non_blocking=True)
+                ev_out[layer].record(cout)
+        main.wait_event(ev_out[L - 1])                    # join both copy streams
+        main.wait_event(ev_in[L - 1])
+
     graphs = {}
     for M in m_list:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(main):
-            dx[M].copy_(hx[M], non_blocking=True)
-            plan.run(dx[M], wp_stack[0], wfb_stack[0], *dout[M], aux_stream=aux, events=evs)
+            calls(M)
         torch.cuda.synchronize()
         with torch.cuda.graph(g, stream=main):
-            for layer in range(L):
-                dx[M].copy_(hx[M], non_blocking=True)
-                plan.run(dx[M], wp_stack[layer], wfb_stack[layer], *dout[M], aux_stream=aux,
-                         events=evs)
-                for d, h in zip(dout[M], hout[M]):
-                    h.copy_(d, non_blocking=True)
+            calls(M)
         graphs[M] = g
     steps = max(1, args.cmp_steps)
     tot = {M: 0.0 for M in m_list}
