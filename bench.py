@@ -274,6 +274,8 @@ def run_ours(args):
     e2e = run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist)
     ex = None if args.no_extras else run_ex(args, wp_stack, dev, main, hbm_peak, dist)
     prefill = None if args.no_extras else run_prefill(args, wp_stack, dev, main, tc_peak_burst, dist)
+    handoff = None if args.no_extras else run_handoff(args, plan, wp_stack, wfb_stack, xs, outs, dev,
+                                                      main, aux, evs, dist)
     clock_info = clocks.stop()
 
     # reductions (max over ranks)
@@ -359,6 +361,7 @@ def run_ours(args):
             "gpu_launches": n_launches,
             "skinny_gemm_ex": ex,
             "prefill": prefill,
+            "pdl_handoff": handoff,
             "clocks": clock_info,
         }
         print(json.dumps(line))
@@ -458,6 +461,49 @@ def run_prefill(args, wp_stack, dev, main, tc_peak, dist, m_pre=(256, 1024, 4096
             row["per_256_slices" if sliced else "one_launch"] = {
                 "us_per_call": round(us, 2), "tflops": round(tf, 1),
                 "frac_of_tensor_peak": round(tf / tc_peak, 4)}
+        out["per_m"][str(M)] = row
+    return out
+
+
+def run_handoff(args, plan, wp_stack, wfb_stack, xs, outs, dev, main, aux, evs, dist, m_h=(1, 16)):
+    """A downstream kernel after every projection call (it reads all of
+    out_qkvg), launched with programmatic dependent launch or without: the
+    difference is the part of its launch and prologue that overlaps the
+    projection's tail. Device time per (projection + consumer) pair."""
+    import torch
+    from decode_projection_gemms_gb300 import binding
+    L = args.layers
+    acc = torch.zeros(1, dtype=torch.int64, device=dev)
+    out = {"consumer": "reads out_qkvg (M x 4096 bf16) after griddepcontrol.wait", "per_m": {}}
+    for M in m_h:
+        if M not in xs:
+            continue
+        oq, of, ob = outs[M]
+        row = {}
+        for pdl in (True, False):
+            def body():
+                for layer in range(L):
+                    plan.run(xs[M], wp_stack[layer], wfb_stack[layer], oq, of, ob,
+                             aux_stream=aux, events=evs)
+                    binding.pdl_consumer_checksum(oq, acc, pdl=pdl)
+            with torch.cuda.stream(main):
+                body()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=main):
+                body()
+            reps = max(2, args.cmp_steps // 2)
+            with torch.cuda.stream(main):
+                g.replay()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(main)
+                for _ in range(reps):
+                    g.replay()
+                b.record(main)
+            torch.cuda.synchronize()
+            us = reduce_max([a.elapsed_time(b)], dist)[0] * 1e3 / (reps * L)
+            row["pdl" if pdl else "no_pdl"] = round(us, 3)
         out["per_m"][str(M)] = row
     return out
 

@@ -37,7 +37,7 @@ EXPORTS = (
     "kda_proj_plan", "kda_proj_set_overlap", "kda_proj_get_config", "kda_proj_set_config",
     "kda_proj_overlap_at", "kda_proj_run", "kda_proj_destroy", "kp_last_error", "kp_version",
     "kp_device_error", "kp_scratch_bytes", "skinny_gemm_noalloc", "skinny_gemm_ex",
-    "kp_selftest_timeout",
+    "kp_selftest_timeout", "kp_pdl_consumer_checksum",
 )
 DEV_SELFTEST = 5   # device error code of kp_selftest_timeout
 
@@ -102,6 +102,7 @@ def load(path: str | None = None):
             "skinny_gemm_noalloc": [vp, vp, vp, ci, ci, ci, cfgp, vp],
             "skinny_gemm_ex": [vp, vp, vp, vp, ci, ci, ci, ci, cfgp, vp],
             "kp_selftest_timeout": [ci, vp],
+            "kp_pdl_consumer_checksum": [vp, ctypes.c_int64, vp, ci, vp],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -168,6 +169,18 @@ def scratch_bytes(M: int, N: int, K: int, cfg: KpCfg, num_sms: int) -> int:
 def selftest_timeout(timeout_us: int = 2000, stream=None):
     """Launch the failure-path self-test (a wait that must run out)."""
     _check(load().kp_selftest_timeout(int(timeout_us), _stream_handle(stream)))
+
+
+def pdl_consumer_checksum(t: torch.Tensor, out: torch.Tensor, pdl: bool = True, stream=None):
+    """Launch the dependent checksum kernel on ``t`` (bf16/fp16, contiguous)
+    adding into ``out`` (a CUDA int64 tensor of one element); ``pdl`` launches
+    it with programmatic stream serialisation."""
+    if t.dtype not in _DTYPES or not t.is_contiguous() or not t.is_cuda:
+        raise TypeError("t must be a contiguous CUDA bf16/fp16 tensor")
+    if out.dtype != torch.int64 or out.numel() != 1 or not out.is_cuda:
+        raise TypeError("out must be a one-element CUDA int64 tensor")
+    _check(load().kp_pdl_consumer_checksum(t.data_ptr(), t.numel(), out.data_ptr(), int(bool(pdl)),
+                                           _stream_handle(stream)))
 
 
 def device_error() -> int:

@@ -358,6 +358,43 @@ int kp_selftest_timeout(int timeout_us, kp_stream_t stream) {
     return KP_OK;
 }
 
+// A dependent kernel (programmatic stream serialisation): lets its own
+// dependents launch, waits for its predecessor, then adds the 16-bit patterns
+// of n elements into *out, exactly.
+__global__ void pdl_consumer_kernel(const uint16_t *buf, int64_t n, unsigned long long *out) {
+    pdl_trigger();
+    pdl_wait();
+    unsigned long long s = 0;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        s += buf[i];
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if ((threadIdx.x & 31) == 0) atomicAdd(out, s);
+}
+
+int kp_pdl_consumer_checksum(const void *buf, int64_t n, unsigned long long *out, int pdl,
+                             kp_stream_t stream) {
+    if (!out || n < 0 || (n > 0 && !buf))
+        return set_error(KP_EINVAL, "kp_pdl_consumer_checksum: bad arguments");
+    if (reinterpret_cast<uintptr_t>(buf) & 1u)
+        return set_error(KP_EALIGN, "kp_pdl_consumer_checksum: buffer must be 2-byte aligned");
+    DevState *d = nullptr;
+    int rc = device_state(&d);
+    if (rc) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(d->sms), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, pdl_consumer_kernel, static_cast<const uint16_t *>(buf), n, out);
+    if (e != cudaSuccess) return cuda_fail(e, "kp_pdl_consumer_checksum launch");
+    return KP_OK;
+}
+
 int kp_device_error(int *code) {
     if (!code) return set_error(KP_EINVAL, "kp_device_error: NULL");
     DevState *d = nullptr;

@@ -291,6 +291,16 @@ KP_API int kp_device_error(int *code);
  * and the kernel exits; the context stays usable. Not part of the
  * projections. Returns KP_OK, KP_EINVAL, KP_ENODEV or KP_ECUDA. */
 KP_API int kp_selftest_timeout(int timeout_us, kp_stream_t stream);
+/* Hand-off check for downstream kernels: launches on `stream` (with
+ * programmatic stream serialisation when pdl != 0) a kernel that executes
+ * griddepcontrol.wait and then adds the 16-bit patterns of buf[0 .. n) into
+ * *out (device, unsigned 64-bit, exact). This library's kernels let such
+ * dependents launch as soon as their own resources are set up, so a consumer
+ * of kda_proj_run's outputs starts its prologue during the projection's tail;
+ * after the wait it sees the outputs complete. buf: device, 2-byte aligned.
+ * Returns KP_OK, KP_EINVAL, KP_EALIGN, KP_ENODEV or KP_ECUDA. */
+KP_API int kp_pdl_consumer_checksum(const void *buf, int64_t n, unsigned long long *out, int pdl,
+                                    kp_stream_t stream);
 /* Bytes of scratch a configuration needs for (M, N, K), for tests/tools. */
 KP_API int kp_scratch_bytes(int M, int N, int K, const kp_cfg *cfg, int num_sms, size_t *bytes);
 

@@ -66,6 +66,8 @@ def test_argument_errors_need_no_device(lib):
     assert lib.kda_proj_plan(7168, 4096, 136, 1024, 0, ctypes.byref(out)) == binding.KP_EINVAL
     assert lib.kda_proj_destroy(None) == binding.KP_OK
     assert lib.kda_proj_set_overlap(None, 0) == binding.KP_ENOPLAN
+    assert lib.kp_pdl_consumer_checksum(p, 4, None, 1, None) == binding.KP_EINVAL
+    assert lib.kp_pdl_consumer_checksum(ctypes.c_void_p(17), 4, p, 1, None) == binding.KP_EALIGN
     assert lib.kp_selftest_timeout(0, None) == binding.KP_EINVAL
     assert lib.kp_selftest_timeout(2000000, None) == binding.KP_EINVAL
     # skinny_gemm_ex: element type and residual alignment, checked before any device work
