@@ -509,53 +509,58 @@ def run_handoff(args, plan, wp_stack, wfb_stack, xs, outs, dev, main, aux, evs, 
 
 
 def run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist):
-    """Same metric through the public API with host buffers: every call copies
-    its x from pinned host memory and its three outputs back. The copies run
-    on two side streams with double-buffered device buffers, so call i's
-    outputs go back and call i+1's x comes in while the device computes."""
+    """Same metric through the public API with host buffers: every call has
+    its own x in pinned host memory and its own output block (the three
+    outputs are consecutive slices of one block), and every call's x goes to
+    the device and its outputs come back inside the timed region. The calls
+    run in chunks: a chunk's inputs go over in one copy on a side stream
+    while the previous chunk computes, and its outputs come back in one copy
+    on another side stream while the next chunk computes. Small M, where a
+    copy's fixed cost dominates, takes the whole chain as one chunk."""
     import torch
     from decode_projection_gemms_gb300.inputs import gen_x
     L = args.layers
+    NOUT = N_QKVG + N_FAB + N_FB
     cin = torch.cuda.Stream(device=dev)
     cout = torch.cuda.Stream(device=dev)
-    hx = {M: gen_x(M, K, seed=M).pin_memory() for M in m_list}
-    dx = {M: [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-          for M in m_list}
-    dout = {M: [(torch.empty((M, N_QKVG), dtype=torch.bfloat16, device=dev),
-                 torch.empty((M, N_FAB), dtype=torch.bfloat16, device=dev),
-                 torch.empty((M, N_FB), dtype=torch.bfloat16, device=dev)) for _ in range(2)]
-            for M in m_list}
-    hout = {M: tuple(torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in dout[M][0])
-            for M in m_list}
+    hx = {M: gen_x(L * M, K, seed=M).view(L, M, K).pin_memory() for M in m_list}
+    dx = {M: torch.empty((L, M, K), dtype=torch.bfloat16, device=dev) for M in m_list}
+    dblk = {M: torch.empty((L, M * NOUT), dtype=torch.bfloat16, device=dev) for M in m_list}
+    hblk = {M: torch.empty((L, M * NOUT), dtype=torch.bfloat16).pin_memory() for M in m_list}
+
+    def chunk_of(M):
+        return L if M <= 4 else min(L, 8)
+
+    def outs(M, layer):
+        flat = dblk[M][layer]
+        a, b = M * N_QKVG, M * (N_QKVG + N_FAB)
+        return (flat[:a].view(M, N_QKVG), flat[a:b].view(M, N_FAB), flat[b:].view(M, N_FB))
 
     def calls(M):
-        ev_in = [torch.cuda.Event() for _ in range(L)]
-        ev_run = [torch.cuda.Event() for _ in range(L)]
-        ev_out = [torch.cuda.Event() for _ in range(L)]
+        CH = chunk_of(M)
+        bounds = [(c, min(c + CH, L)) for c in range(0, L, CH)]
+        ev_in = [torch.cuda.Event() for _ in bounds]
+        ev_run = [torch.cuda.Event() for _ in bounds]
         start = torch.cuda.Event()
         start.record(main)
         cin.wait_event(start)
         cout.wait_event(start)
-        for layer in range(L):
-            b = layer % 2
-            with torch.cuda.stream(cin):
-                if layer >= 2:
-                    cin.wait_event(ev_run[layer - 2])     # dx[b] is free again
-                dx[M][b].copy_(hx[M], non_blocking=True)
-                ev_in[layer].record(cin)
-            main.wait_event(ev_in[layer])
-            if layer >= 2:
-                main.wait_event(ev_out[layer - 2])        # dout[b] has been read back
-            plan.run(dx[M][b], wp_stack[layer], wfb_stack[layer], *dout[M][b],
-                     aux_stream=aux, events=evs)
-            ev_run[layer].record(main)
+        with torch.cuda.stream(cin):
+            for i, (a, b) in enumerate(bounds):
+                dx[M][a:b].copy_(hx[M][a:b], non_blocking=True)
+                ev_in[i].record(cin)
+        for i, (a, b) in enumerate(bounds):
+            main.wait_event(ev_in[i])
+            for layer in range(a, b):
+                plan.run(dx[M][layer], wp_stack[layer], wfb_stack[layer], *outs(M, layer),
+                         aux_stream=aux, events=evs)
+            ev_run[i].record(main)
             with torch.cuda.stream(cout):
-                cout.wait_event(ev_run[layer])
-                for d, h in zip(dout[M][b], hout[M]):
-                    h.copy_(d, non_blocking=True)
-                ev_out[layer].record(cout)
-        main.wait_event(ev_out[L - 1])                    # join both copy streams
-        main.wait_event(ev_in[L - 1])
+                cout.wait_event(ev_run[i])
+                hblk[M][a:b].copy_(dblk[M][a:b], non_blocking=True)
+        end = torch.cuda.Event()
+        end.record(cout)
+        main.wait_event(end)                              # join the copy streams
 
     graphs = {}
     for M in m_list:
@@ -582,13 +587,17 @@ def run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist):
                 b.record(main)
                 b.synchronize()
                 tot[M] += a.elapsed_time(b)
+    # the host copy of the last call's outputs is what the device wrote
+    for M in m_list:
+        assert torch.equal(hblk[M][L - 1], dblk[M][L - 1].cpu()), f"e2e read-back mismatch at M={M}"
     vals = reduce_max([tot[M] for M in m_list], dist)
     us = [v * 1e3 / (steps * L) for v in vals]
     h2d = sum(M * K * 2 for M in m_list) * L
-    d2h = sum(M * (N_QKVG + N_FAB + N_FB) * 2 for M in m_list) * L
+    d2h = sum(M * NOUT * 2 for M in m_list) * L
     return {"value": round(statistics.fmean(us), 3), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "per_m_us": {str(M): round(u, 3) for M, u in zip(m_list, us)}}
+            "per_m_us": {str(M): round(u, 3) for M, u in zip(m_list, us)},
+            "calls_per_copy": {str(M): chunk_of(M) for M in m_list}}
 
 
 # ---------------------------------------------------------------------------
