@@ -95,6 +95,7 @@ struct Tc05Params {
     uint32_t tmem_cols;
     uint32_t stage_bytes;
     uint32_t w_stage_bytes;
+    int vec4;          // 1: y and y2 take 8-byte stores of four features
 };
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, stride byte
@@ -401,14 +402,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // All partial tiles of the cluster are in shared memory after this.
         __syncwarp();
         cluster_sync_all();
+        // This CTA reduces rows r0 .. r0 + rpc - 1 of the tile for every
+        // token. A thread owns four of those rows (rr .. rr + 3) and walks
+        // the tokens m = t / groups, + mstep, ...: the rows and the output
+        // row pointer are fixed per thread, so a token costs C remote loads,
+        // the rank-order sums and one store.
         const int rpc = RT / C;                 // rows reduced by this CTA (>= 8)
-        const int groups = rpc / 4;             // float4 groups per token
-        const int r0 = rank * rpc;
-        const uint32_t red_base = base;         // same offset in every CTA
-        for (int idx = threadIdx.x; idx < Mloc * groups; idx += kThreads) {
-            const int m = idx / groups;
-            const int rr = r0 + 4 * (idx - m * groups);
-            const uint32_t off = red_base + static_cast<uint32_t>((m * RT + rr) * 4);
+        const int lg_groups = 29 - __clz(rpc);  // log2(rpc / 4): float4 groups per token
+        const int g = threadIdx.x & ((1 << lg_groups) - 1);
+        const int mstep = kThreads >> lg_groups;   // groups (<= 64) divides 192
+        const int rr = rank * rpc + 4 * g;
+        const int nb = tile * RT + rr;
+        // output row for features nb .. nb + 3 (one side of n_split, a multiple of 128)
+        const bool lo = nb < p.n_split;
+        uint16_t *const yrow = reinterpret_cast<uint16_t *>(lo ? p.y : p.y2) + (lo ? nb : nb - p.n_split);
+        const int64_t ldo = lo ? p.ldy : p.ldy2;
+        const bool whole = p.vec4 && nb + 3 < p.N;
+        for (int m = threadIdx.x >> lg_groups; m < Mloc; m += mstep) {
+            const uint32_t off = base + static_cast<uint32_t>((m * RT + rr) * 4);
             float4 part[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c)
@@ -422,29 +433,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     acc.z += part[c].z;
                     acc.w += part[c].w;
                 }
-            const int nb = tile * RT + rr;
-            uint32_t b0, b1, b2, b3;
+            uint32_t w0, w1;   // bf16 bits of rows rr, rr+1 and rr+2, rr+3
             if constexpr (kGeneral) {
-                b0 = nb + 0 < p.N ? finish(p, m0 + m, nb + 0, acc.x) : 0;
-                b1 = nb + 1 < p.N ? finish(p, m0 + m, nb + 1, acc.y) : 0;
-                b2 = nb + 2 < p.N ? finish(p, m0 + m, nb + 2, acc.z) : 0;
-                b3 = nb + 3 < p.N ? finish(p, m0 + m, nb + 3, acc.w) : 0;
+                uint32_t b[4];
+                const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) b[e] = nb + e < p.N ? finish(p, m0 + m, nb + e, v[e]) : 0;
+                w0 = b[0] | (b[1] << 16);
+                w1 = b[2] | (b[3] << 16);
             } else {
-                b0 = bf16_bits_rn(acc.x);
-                b1 = bf16_bits_rn(acc.y);
-                b2 = bf16_bits_rn(acc.z);
-                b3 = bf16_bits_rn(acc.w);
-                if (nb + 0 < p.N) store_bits(p, m0 + m, nb + 0, b0);
-                if (nb + 1 < p.N) store_bits(p, m0 + m, nb + 1, b1);
-                if (nb + 2 < p.N) store_bits(p, m0 + m, nb + 2, b2);
-                if (nb + 3 < p.N) store_bits(p, m0 + m, nb + 3, b3);
+                const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x, acc.y);
+                const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z, acc.w);
+                w0 = *reinterpret_cast<const uint32_t *>(&h0);
+                w1 = *reinterpret_cast<const uint32_t *>(&h1);
+                uint16_t *const dst = yrow + (m0 + m) * ldo;
+                if (whole) {
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(w0, w1);
+                } else {
+                    if (nb + 0 < p.N) dst[0] = static_cast<uint16_t>(w0);
+                    if (nb + 1 < p.N) dst[1] = static_cast<uint16_t>(w0 >> 16);
+                    if (nb + 2 < p.N) dst[2] = static_cast<uint16_t>(w1);
+                    if (nb + 3 < p.N) dst[3] = static_cast<uint16_t>(w1 >> 16);
+                }
             }
             if (fused && rr < kTileN) {
                 // this rank's features rr..rr+3 of the F_B operand (8 bytes),
                 // written into its own copy and into every CTA of the cluster
                 // that computes F_B tiles (the F_B operand region lies past
                 // the partial tiles, so no reader is disturbed)
-                const uint2 pk = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+                const uint2 pk = make_uint2(w0, w1);
                 const uint32_t off = base + p.off_bfa + bfa_offset(m, rr, p.Mpad);
                 *reinterpret_cast<uint2 *>(gbase + p.off_bfa + bfa_offset(m, rr, p.Mpad)) = pk;
                 for (int c = 0; c < C && c < p.fb_tiles; ++c)
@@ -777,6 +794,9 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     p.tmem_cols = tmem_cols_of(rt / kTileN * Mpad);   // one accumulator per 128-row half
     p.stage_bytes = stage_bytes_of(Mpad, nkb, rt);
     p.w_stage_bytes = w_stage_bytes_of(nkb, rt);
+    p.vec4 = (p.ldy % 4 == 0 && (reinterpret_cast<uintptr_t>(p.y) & 7) == 0 &&
+              (!p.y2 || (p.ldy2 % 4 == 0 && (reinterpret_cast<uintptr_t>(p.y2) & 7) == 0)))
+                 ? 1 : 0;
     p.fb_tile = -1;
     p.fb_tiles = 0;
     p.N_fb = 0;
