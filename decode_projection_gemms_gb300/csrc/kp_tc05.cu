@@ -42,6 +42,7 @@
 #include <cstring>
 #include <mutex>
 #include <set>
+#include <type_traits>
 #include <utility>
 
 #include "kp_internal.cuh"
@@ -467,48 +468,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             a.w += b.w;
         };
         const int mfirst = threadIdx.x >> lg_groups;
-        if (C <= 4) {
-            // two tokens per pass: 2 * C remote loads in flight together
-            for (int m = mfirst; m < Mloc; m += 2 * mstep) {
-                const int m2 = m + mstep;
-                const uint32_t off = base + static_cast<uint32_t>((m * RT + rr) * 4);
-                const uint32_t off2 = off + static_cast<uint32_t>(mstep * RT * 4);
-                float4 pa[4], pb[4];
+        // T tokens per pass with up to CM peers each: T * CM remote loads
+        // in flight together before their sums (two tokens measured best
+        // up to clusters of 8; four were slower at C = 4).
+        auto passes = [&](auto t_c, auto cm_c) {
+            constexpr int T = decltype(t_c)::value;
+            constexpr int CM = decltype(cm_c)::value;
+            for (int m = mfirst; m < Mloc; m += T * mstep) {
+                float4 part[T][CM];
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    if (c < C) pa[c] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(c)));
-                if (m2 < Mloc) {
+                for (int t = 0; t < T; ++t) {
+                    const int mt = m + t * mstep;
+                    if (mt < Mloc) {
+                        const uint32_t off = base + static_cast<uint32_t>((mt * RT + rr) * 4);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (c < C) pb[c] = ld_dsmem_f4(mapa_shared(off2, static_cast<uint32_t>(c)));
+                        for (int c = 0; c < CM; ++c)
+                            if (c < C) part[t][c] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(c)));
+                    }
                 }
-                float4 acc = pa[0];
 #pragma unroll
-                for (int c = 1; c < 4; ++c)
-                    if (c < C) add4(acc, pa[c]);
-                emit(m, acc);
-                if (m2 < Mloc) {
-                    acc = pb[0];
+                for (int t = 0; t < T; ++t) {
+                    const int mt = m + t * mstep;
+                    if (mt < Mloc) {
+                        float4 acc = part[t][0];
 #pragma unroll
-                    for (int c = 1; c < 4; ++c)
-                        if (c < C) add4(acc, pb[c]);
-                    emit(m2, acc);
+                        for (int c = 1; c < CM; ++c)
+                            if (c < C) add4(acc, part[t][c]);
+                        emit(mt, acc);
+                    }
                 }
             }
-        } else {
-            for (int m = mfirst; m < Mloc; m += mstep) {
-                const uint32_t off = base + static_cast<uint32_t>((m * RT + rr) * 4);
-                float4 part[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    if (c < C) part[c] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(c)));
-                float4 acc = part[0];
-#pragma unroll
-                for (int c = 1; c < 16; ++c)
-                    if (c < C) add4(acc, part[c]);
-                emit(m, acc);
-            }
-        }
+        };
+        if (C <= 4)
+            passes(std::integral_constant<int, 2>(), std::integral_constant<int, 4>());
+        else if (C <= 8)
+            passes(std::integral_constant<int, 2>(), std::integral_constant<int, 8>());
+        else
+            passes(std::integral_constant<int, 1>(), std::integral_constant<int, 16>());
         // Written F_B operand slices reach the tensor cores' (async) proxy of
         // whichever CTA reads them after the barrier.
         if (fused) asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
