@@ -88,6 +88,15 @@ def test_ex_tc05_large_m(dtype, M):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("M", [3, 128])
+def test_ex_tc05_odd_n(dtype, M):
+    # the general epilogue's split-K reduction with N not a multiple of 4
+    x, W, r = case(M, 1001, 2048, dtype, seed=M + 5)
+    for C in (2, 8):
+        check_ex(x, W, r, dtype, KpCfg.make("tc05", split_k=C, k_unroll=1, stages=2), f"tc05 C={C}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("M", [1, 33])
 def test_ex_smallk(dtype, M):
     x, W, r = case(M, 1024, 128, dtype, seed=70 + M)

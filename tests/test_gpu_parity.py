@@ -119,6 +119,19 @@ def test_tc05_cluster_splits(C, nkb):
                    f"tc05 P={P}")
 
 
+@pytest.mark.parametrize("N", [7, 131, 1001])
+@pytest.mark.parametrize("C", [2, 4, 8])
+@pytest.mark.parametrize("M", [1, 37, 128])
+def test_tc05_odd_n(M, C, N):
+    # N not a multiple of 4: the split-K reduction stores element by element,
+    # and the last tile ends inside a group of four rows
+    x, W = gemm_case(M, N, 2048, seed=M + C + N)
+    cfg = KpCfg.make("tc05", split_k=C, k_unroll=1, stages=2)
+    if not _tc05_ok(M, N, 2048, cfg):
+        pytest.skip("does not fit")
+    check_gemm(x, W, cfg, "tc05 odd N")
+
+
 def test_tc05_m_above_256_two_token_tiles():
     x, W = gemm_case(300, 264, 512, seed=8)
     check_gemm(x, W, KpCfg.make("tc05", split_k=4, k_unroll=1), "tc05")
