@@ -422,44 +422,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Round the sum of rows rr .. rr + 3 for token m, store it, and
         // (fused tile) hand it to the F_B operand.
         auto emit = [&](int m, const float4 &acc) {
-                uint32_t w0, w1;   // bf16 bits of rows rr, rr+1 and rr+2, rr+3
-                if constexpr (kGeneral) {
-                    uint32_t b[4];
-                    const float v[4] = {acc.x, acc.y, acc.z, acc.w};
-    #pragma unroll
-                    for (int e = 0; e < 4; ++e) b[e] = nb + e < p.N ? finish(p, m0 + m, nb + e, v[e]) : 0;
-                    w0 = b[0] | (b[1] << 16);
-                    w1 = b[2] | (b[3] << 16);
+            uint32_t w0, w1;   // bf16 bits of rows rr, rr+1 and rr+2, rr+3
+            if constexpr (kGeneral) {
+                uint32_t b[4];
+                const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) b[e] = nb + e < p.N ? finish(p, m0 + m, nb + e, v[e]) : 0;
+                w0 = b[0] | (b[1] << 16);
+                w1 = b[2] | (b[3] << 16);
+            } else {
+                const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x, acc.y);
+                const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z, acc.w);
+                w0 = *reinterpret_cast<const uint32_t *>(&h0);
+                w1 = *reinterpret_cast<const uint32_t *>(&h1);
+                uint16_t *const dst = yrow + (m0 + m) * ldo;
+                if (whole) {
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(w0, w1);
                 } else {
-                    const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x, acc.y);
-                    const __nv_bfloat162 h1 = __floats2bfloat162_rn(acc.z, acc.w);
-                    w0 = *reinterpret_cast<const uint32_t *>(&h0);
-                    w1 = *reinterpret_cast<const uint32_t *>(&h1);
-                    uint16_t *const dst = yrow + (m0 + m) * ldo;
-                    if (whole) {
-                        *reinterpret_cast<uint2 *>(dst) = make_uint2(w0, w1);
-                    } else {
-                        if (nb + 0 < p.N) dst[0] = static_cast<uint16_t>(w0);
-                        if (nb + 1 < p.N) dst[1] = static_cast<uint16_t>(w0 >> 16);
-                        if (nb + 2 < p.N) dst[2] = static_cast<uint16_t>(w1);
-                        if (nb + 3 < p.N) dst[3] = static_cast<uint16_t>(w1 >> 16);
-                    }
+                    if (nb + 0 < p.N) dst[0] = static_cast<uint16_t>(w0);
+                    if (nb + 1 < p.N) dst[1] = static_cast<uint16_t>(w0 >> 16);
+                    if (nb + 2 < p.N) dst[2] = static_cast<uint16_t>(w1);
+                    if (nb + 3 < p.N) dst[3] = static_cast<uint16_t>(w1 >> 16);
                 }
-                if (fused && rr < kTileN) {
-                    // this rank's features rr..rr+3 of the F_B operand (8 bytes),
-                    // written into its own copy and into every CTA of the cluster
-                    // that computes F_B tiles (the F_B operand region lies past
-                    // the partial tiles, so no reader is disturbed)
-                    const uint2 pk = make_uint2(w0, w1);
-                    const uint32_t off = base + p.off_bfa + bfa_offset(m, rr, p.Mpad);
-                    *reinterpret_cast<uint2 *>(gbase + p.off_bfa + bfa_offset(m, rr, p.Mpad)) = pk;
-                    for (int c = 0; c < C && c < p.fb_tiles; ++c)
-                        if (c != rank)
-                            asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(
-                                             mapa_shared(off, static_cast<uint32_t>(c))),
-                                         "r"(pk.x), "r"(pk.y)
-                                         : "memory");
-                }
+            }
+            if (fused && rr < kTileN) {
+                // this rank's features rr..rr+3 of the F_B operand (8 bytes),
+                // written into its own copy and into every CTA of the cluster
+                // that computes F_B tiles (the F_B operand region lies past
+                // the partial tiles, so no reader is disturbed)
+                const uint2 pk = make_uint2(w0, w1);
+                const uint32_t off = base + p.off_bfa + bfa_offset(m, rr, p.Mpad);
+                *reinterpret_cast<uint2 *>(gbase + p.off_bfa + bfa_offset(m, rr, p.Mpad)) = pk;
+                for (int c = 0; c < C && c < p.fb_tiles; ++c)
+                    if (c != rank)
+                        asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(
+                                         mapa_shared(off, static_cast<uint32_t>(c))),
+                                     "r"(pk.x), "r"(pk.y)
+                                     : "memory");
+            }
         };
         auto add4 = [](float4 &a, const float4 &b) {
             a.x += b.x;
