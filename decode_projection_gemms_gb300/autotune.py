@@ -400,6 +400,8 @@ def main(argv=None):
         swept = set(shapes)
         keep = []
         for line in open(args.append_to):
+            if line.startswith("# shape sweep"):
+                continue   # replaced by the new sweep's header below
             f = line.split("#")[0].split()
             if len(f) >= 3 and (int(f[1]), int(f[2])) in swept:
                 continue
