@@ -273,10 +273,19 @@ def run_ours(args):
         tot_q, _ = timed(graphs_q, args.cmp_steps)
     e2e = run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist)
     ex = None if args.no_extras else run_ex(args, wp_stack, dev, main, hbm_peak, dist)
+    cc = None if args.no_extras else run_cuda_core(args, wp_stack, dev, main, hbm_peak, dist)
     prefill = None if args.no_extras else run_prefill(args, wp_stack, dev, main, tc_peak_burst, dist)
     handoff = None if args.no_extras else run_handoff(args, plan, wp_stack, wfb_stack, xs, outs, dev,
                                                       main, aux, evs, dist)
     clock_info = clocks.stop()
+    if cc is not None:
+        # FP32-pipe roofline: 128 FMA lanes per SM at the highest SM clock seen
+        mhz = clock_info.get("sm_max_mhz") or 2070.0
+        alu_peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * mhz * 1e6
+        cc["alu_peak_fma_per_s"] = alu_peak
+        for row in cc["per_m"].values():
+            row["frac_of_alu_peak"] = round(row["fma_per_s"] / alu_peak, 4)
+            row["fma_per_s"] = round(row["fma_per_s"], -6)
 
     # reductions (max over ranks)
     keys = list(m_list)
@@ -325,6 +334,10 @@ def run_ours(args):
         return 2 if fused else 3
     q_bytes = sum(qkvg_bytes(M) for M in keys)
     q_time_us = sum(per_m[str(M)]["qkvg_kernel_us"] for M in keys)
+    if cc is not None:
+        for Ms, row in cc["per_m"].items():
+            if Ms in per_m:   # the tcgen05 kernel on the same shape, same run
+                row["tcgen05_us"] = per_m[Ms]["qkvg_kernel_us"]
     achieved = q_bytes / (q_time_us * 1e3)  # GB/s
     n_launches = args.steps * L * sum(launches_per_call(M) for M in keys)
     cpu = run_cpu_baseline(args, m_list) if (rank == 0 and not args.no_cpu) else None
@@ -360,6 +373,7 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": n_launches,
             "skinny_gemm_ex": ex,
+            "cuda_core_splitk": cc,
             "prefill": prefill,
             "pdl_handoff": handoff,
             "clocks": clock_info,
@@ -411,6 +425,64 @@ def run_ex(args, wp_stack, dev, main, hbm_peak, dist, m_ex=(1, 16)):
                             "frac_of_roofline": round(nbytes / (us * 1e3) / hbm_peak, 4)}
         out["per_m"][str(M)] = row
     del stacks
+    return out
+
+
+def run_cuda_core(args, wp_stack, dev, main, hbm_peak, dist, m_cc=(1, 4, 8, 16)):
+    """The CUDA-core split-K GEMV at the Q/K/V/G shape (N=4096, K=7168), the
+    kernel kind the projection would use at M <= 16 without the tcgen05
+    kernel: the fastest of its candidate configurations per M (short runs,
+    then the winner re-timed), as a graph of one call per layer of the
+    rotated weight stack. Reports the HBM fraction and the FMA rate (M*N*K
+    fused multiply-adds per call) for the FP32-pipe roofline."""
+    import torch
+    from decode_projection_gemms_gb300 import binding
+    from decode_projection_gemms_gb300.autotune import cc_candidates
+    from decode_projection_gemms_gb300.inputs import gen_x
+
+    L = wp_stack.shape[0]
+    W = wp_stack[:, :N_QKVG]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {"shape": {"N": N_QKVG, "K": K}, "layers": L, "per_m": {}}
+
+    def time_cfg(x, y, cfg, reps):
+        with torch.cuda.stream(main):
+            binding.skinny_gemm(x, W[0], y, cfg=cfg)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            for layer in range(L):
+                binding.skinny_gemm(x, W[layer], y, cfg=cfg)
+        with torch.cuda.stream(main):
+            g.replay()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            for _ in range(reps):
+                g.replay()
+            b.record(main)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * L)
+
+    for M in m_cc:
+        x = gen_x(M, K, seed=3).to(dev)
+        y = torch.empty((M, N_QKVG), dtype=torch.bfloat16, device=dev)
+        best = None
+        for cfg in cc_candidates(M, N_QKVG, K, sms):
+            try:
+                binding.scratch_bytes(M, N_QKVG, K, cfg, sms)
+            except binding.KdaProjError:
+                continue
+            us = time_cfg(x, y, cfg, 2)
+            if best is None or us < best[0]:
+                best = (us, cfg)
+        us = reduce_max([time_cfg(x, y, best[1], args.cmp_steps)], dist)[0]
+        nbytes = qkvg_bytes(M)
+        out["per_m"][str(M)] = {"us_per_call": round(us, 3), "gbs": round(nbytes / (us * 1e3), 1),
+                                "frac_of_hbm_roofline": round(nbytes / (us * 1e3) / hbm_peak, 4),
+                                "fma_per_s": M * N_QKVG * K / (us * 1e-6),
+                                "config": best[1].as_dict()}
+    del W
     return out
 
 
