@@ -482,7 +482,6 @@ def run_cuda_core(args, wp_stack, dev, main, hbm_peak, dist, m_cc=(1, 4, 8, 16))
                                 "frac_of_hbm_roofline": round(nbytes / (us * 1e3) / hbm_peak, 4),
                                 "fma_per_s": M * N_QKVG * K / (us * 1e-6),
                                 "config": best[1].as_dict()}
-    del W
     return out
 
 
