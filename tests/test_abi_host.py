@@ -164,6 +164,23 @@ def test_scratch_sizes(lib):
     assert e.value.code == binding.KP_ECONFIG
 
 
+def test_partial_tile_must_fit_the_stages(lib):
+    # C > 1 reduces an Mpad x 128 fp32 partial tile in the stage memory: at
+    # M = 128 that is 64 KB, so one 32 KB stage (one K block: 16 KB W + 16 KB x)
+    # is too small and two are enough; C = 1 has no partial tile
+    def ok(M, C, stages):
+        try:
+            binding.scratch_bytes(M, 4096, 7168, binding.KpCfg.make(
+                "tc05", split_k=C, k_unroll=1, stages=stages), 152)
+            return True
+        except binding.KdaProjError as e:
+            assert e.code == binding.KP_ECONFIG
+            return False
+    assert not ok(128, 4, 1) and ok(128, 4, 2) and ok(128, 1, 1)
+    # M = 16: 8 KB partial tile, 18 KB stage
+    assert ok(16, 16, 1)
+
+
 def test_fuse_flag_is_plan_only(lib):
     fused = binding.KpCfg.make("tc05", split_k=4, k_unroll=2,
                                flags=binding.FLAG_PDL | binding.FLAG_FUSE_FB)
