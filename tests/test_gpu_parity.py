@@ -2,8 +2,9 @@
 
 Tolerance (bf16 output, fp32 accumulation): |gpu - ref| <= 4 ulp_bf16(|ref|)
 + 1e-3 per element; outputs are NaN-poisoned before each call so an element a
-kernel never writes fails. F_B's bound adds the propagated F_A tolerance
-(sum_k dF_A[k] |W_fb[n, k]|), which is zero extra whenever F_A matches.
+kernel never writes fails. F_B is checked twice: from the GPU's own bf16 F_A
+at that plain bound (stage-isolated), and end to end from the oracle's F_A,
+where the bound adds the propagated F_A tolerance (sum_k dF_A[k] |W_fb[n, k]|).
 """
 import numpy as np
 import pytest
@@ -14,7 +15,8 @@ from decode_projection_gemms_gb300 import binding
 from decode_projection_gemms_gb300.binding import KpCfg
 from decode_projection_gemms_gb300.inputs import bf16_bits, gen_w, gen_x
 
-from gpu_helpers import check_gemm, check_kda, gemm_case, kda_inputs, poisoned, to_f64
+from gpu_helpers import (check_gemm, check_kda, gemm_case, kda_inputs,
+                         kda_reference, poisoned, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -258,6 +260,49 @@ def test_kda_chain_closed_form():
         assert torch.equal(ob.float().cpu(), torch.full((M, 64), 925696.0))
     finally:
         p.close()
+
+
+# ---- F_B in every schedule, stage-isolated at the plain bound ---------------------------------
+
+@pytest.mark.parametrize("layer", [0, 47])
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_kda_every_mode_against_the_oracle(plan, M, layer):
+    """Sequential, overlapped, single launch, and the aux branch with F_B fused
+    into the F_A/beta launch: every output against the oracle, F_B also from
+    the GPU's own F_A at 4 ulp + 1e-3 with no widening."""
+    x, wp, wfb = kda_inputs(M, layer=layer)
+    ref = kda_reference(x, wp, wfb, 4096, 136)
+    xd, wpd, wfbd = x.cuda(), wp.cuda(), wfb.cuda()
+    aux = torch.cuda.Stream()
+    evs = binding.make_events()
+    saved = plan.get_config(binding.BRANCH_FAB, M)
+    try:
+        for mode in (0, 1, 2):
+            outs = _run_mode(plan, xd, wpd, wfbd, mode, aux, evs)
+            check_kda(outs, x, wp, wfb, 4096, 136, f"mode {mode} M={M} layer {layer}", ref=ref)
+        fused = KpCfg.from_buffer_copy(saved)
+        if fused.kind == binding.KIND_TC05:
+            fused.flags |= binding.FLAG_FUSE_FB
+            try:
+                plan.set_config(binding.BRANCH_FAB, M, fused)
+            except binding.KdaProjError:
+                return   # no room for the F_B operands beside this configuration
+            for mode in (0, 1):
+                outs = _run_mode(plan, xd, wpd, wfbd, mode, aux, evs)
+                check_kda(outs, x, wp, wfb, 4096, 136, f"fused F_B mode {mode} M={M}", ref=ref)
+    finally:
+        plan.set_config(binding.BRANCH_FAB, M, saved)
+        plan.set_overlap(-1)
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 64, 128, 200, 256])
+def test_tc05_f_b_shape_one_cta_per_tile(M):
+    """The fused F_B's MMA sequence (one CTA per 128-row tile, K = 128 in two
+    64-wide K blocks) as a plain GEMM on the F_B shape, against the oracle."""
+    x, W = gemm_case(M, 1024, 128, seed=300 + M)
+    check_gemm(x, W, KpCfg.make("tc05", split_k=1, k_unroll=2), "tc05 F_B shape")
+    x, W = gemm_case(M, 1000, 128, seed=400 + M)
+    check_gemm(x, W, KpCfg.make("tc05", split_k=1, k_unroll=2), "tc05 F_B shape, ragged N")
 
 
 # ---- bit identity: sequential == overlapped == graph replay == PDL off ---------------------
