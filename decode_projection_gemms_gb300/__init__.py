@@ -7,7 +7,7 @@ the library with :func:`decode_projection_gemms_gb300.build.build`.
 from __future__ import annotations
 
 __all__ = ["KdaPlan", "KpCfg", "KdaProjError", "skinny_gemm", "select_config", "make_events",
-           "table_load", "table_clear", "device_error"]
+           "table_load", "table_clear", "device_error", "check_device"]
 
 
 def __getattr__(name):

@@ -19,10 +19,11 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkdaproj.so")
 TABLE_PATH = os.path.join(_HERE, "tune", "gb300_table.txt")
 
 # enum kp_status
-KP_OK, KP_EINVAL, KP_EALIGN, KP_ESHAPE, KP_ENOPLAN, KP_ECUDA, KP_ETOOBIG, KP_ENODEV, KP_ECONFIG, KP_EIO = (
-    0, -1, -2, -3, -4, -5, -6, -7, -8, -9)
+(KP_OK, KP_EINVAL, KP_EALIGN, KP_ESHAPE, KP_ENOPLAN, KP_ECUDA, KP_ETOOBIG, KP_ENODEV, KP_ECONFIG,
+ KP_EIO, KP_EDEVICE) = (0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10)
 STATUS_NAMES = {0: "KP_OK", -1: "KP_EINVAL", -2: "KP_EALIGN", -3: "KP_ESHAPE", -4: "KP_ENOPLAN",
-                -5: "KP_ECUDA", -6: "KP_ETOOBIG", -7: "KP_ENODEV", -8: "KP_ECONFIG", -9: "KP_EIO"}
+                -5: "KP_ECUDA", -6: "KP_ETOOBIG", -7: "KP_ENODEV", -8: "KP_ECONFIG", -9: "KP_EIO",
+                -10: "KP_EDEVICE"}
 # enum kp_kind
 KIND_AUTO, KIND_CC, KIND_TC05, KIND_SMALLK = 0, 1, 2, 3
 KIND_NAMES = {0: "auto", 1: "cc", 2: "tc05", 3: "smallk"}
@@ -184,9 +185,22 @@ def pdl_consumer_checksum(t: torch.Tensor, out: torch.Tensor, pdl: bool = True, 
 
 
 def device_error() -> int:
+    """Read and clear the current device's error word (0: no kernel wait ran
+    out). Does not wait for the device."""
     v = ctypes.c_int()
     _check(load().kp_device_error(ctypes.byref(v)))
     return int(v.value)
+
+
+def check_device(stream=None):
+    """Wait for ``stream`` (default: the current stream), then raise
+    ``KdaProjError(KP_EDEVICE)`` if a kernel wait ran out meanwhile (the
+    outputs of that work are undefined). Reading clears the code."""
+    (stream or torch.cuda.current_stream()).synchronize()
+    code = device_error()
+    if code:
+        raise KdaProjError(KP_EDEVICE, f"a kernel wait ran out (device error code {code}); "
+                                       "the outputs of the work just run are undefined")
 
 
 def skinny_gemm(x: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None,
@@ -309,12 +323,14 @@ class KdaPlan:
 
     def run(self, x: torch.Tensor, W_packed: torch.Tensor, W_fb: torch.Tensor,
             out_qkvg=None, out_fab=None, out_fb=None, aux_stream=None, events=None,
-            stream=None):
+            stream=None, check: bool = False):
         """Enqueue the projection; returns ``(out_qkvg, out_fab, out_fb)``.
 
         ``aux_stream`` (torch.cuda.Stream) and ``events`` (two
         torch.cuda.Event) enable the two-stream overlap; ``stream`` is the
-        main stream (default: the current stream)."""
+        main stream (default: the current stream). ``check=True`` waits for
+        the main stream and raises ``KdaProjError(KP_EDEVICE)`` if a kernel
+        wait ran out during the call (not usable under graph capture)."""
         _bf16_2d(x, "x")
         _bf16_2d(W_packed, "W_packed")
         _bf16_2d(W_fb, "W_fb")
@@ -343,6 +359,8 @@ class KdaPlan:
         _check(self._lib.kda_proj_run(self._h, x.data_ptr(), W_packed.data_ptr(), W_fb.data_ptr(),
                                       out_qkvg.data_ptr(), out_fab.data_ptr(), out_fb.data_ptr(), M,
                                       _stream_handle(stream), aux, ev))
+        if check:
+            check_device(stream)
         return out_qkvg, out_fab, out_fb
 
     def close(self):

@@ -19,8 +19,6 @@
 
 #include "kp_internal.cuh"
 
-__device__ int g_kp_dev_err;
-
 namespace kp {
 
 // ---- errors ---------------------------------------------------------------------
@@ -39,13 +37,28 @@ static int cuda_fail(cudaError_t e, const char *what) {
     return set_error(KP_ECUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
 }
 
+// A kernel wait on this device ran out earlier and nobody has read the code
+// yet: refuse new work (the outputs of that call are undefined).
+static int refuse_after_give_up(const int *err_host) {
+    const int v = err_host ? __atomic_load_n(err_host, __ATOMIC_ACQUIRE) : 0;
+    if (v == 0) return KP_OK;
+    return set_error(KP_EDEVICE,
+                     "a kernel wait on this device ran out earlier (code %d); the outputs of that "
+                     "call are undefined. kp_device_error() reads and clears the code", v);
+}
+
 // ---- per-device state -------------------------------------------------------------
 
 struct DevState {
     bool ok = false;
     int sms = 0;
     int major = 0, minor = 0;
-    int *err = nullptr;       // &g_kp_dev_err on this device
+    // Error word of this device's kernels, in mapped pinned host memory:
+    // kernels write it with system-scope atomics (err), host code reads it
+    // with plain atomics (err_host) and no CUDA call, so an entry point can
+    // refuse new work after a give-up without synchronising.
+    int *err = nullptr;
+    int *err_host = nullptr;
     // skinny_gemm's scratch, grown on demand
     float *ws = nullptr;
     size_t ws_floats = 0;
@@ -70,10 +83,17 @@ static int device_state(DevState **out) {
         if (d.major != 10 || d.minor != 3)
             return set_error(KP_ENODEV, "device %d is sm_%d%d; this library is built for sm_103a",
                              dev, d.major, d.minor);
-        void *p = nullptr;
-        if ((e = cudaGetSymbolAddress(&p, g_kp_dev_err)) != cudaSuccess)
-            return cuda_fail(e, "cudaGetSymbolAddress(error word)");
-        d.err = static_cast<int *>(p);
+        void *h = nullptr;
+        if ((e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable)) != cudaSuccess)
+            return cuda_fail(e, "cudaHostAlloc(error word)");
+        memset(h, 0, 64);
+        void *dp = nullptr;
+        if ((e = cudaHostGetDevicePointer(&dp, h, 0)) != cudaSuccess) {
+            cudaFreeHost(h);
+            return cuda_fail(e, "cudaHostGetDevicePointer(error word)");
+        }
+        d.err_host = static_cast<int *>(h);
+        d.err = static_cast<int *>(dp);
         d.ok = true;
     }
     *out = &d;
@@ -204,7 +224,8 @@ struct kda_plan {
     size_t ws_floats[3] = {0, 0, 0};
     int *cnt[3] = {nullptr, nullptr, nullptr};
     size_t cnt_n[3] = {0, 0, 0};
-    int *err = nullptr;
+    int *err = nullptr;        // the device's error word (device view)
+    int *err_host = nullptr;   // the same word, host view
 };
 
 namespace kp {
@@ -400,13 +421,8 @@ int kp_device_error(int *code) {
     DevState *d = nullptr;
     int rc = device_state(&d);
     if (rc) return rc;
-    int v = 0;
-    cudaError_t e = cudaMemcpy(&v, d->err, sizeof v, cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-    const int zero = 0;
-    e = cudaMemcpy(d->err, &zero, sizeof zero, cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
-    *code = v;
+    // one atomic read-and-clear: a code written meanwhile is never lost
+    *code = __atomic_exchange_n(d->err_host, 0, __ATOMIC_ACQ_REL);
     return KP_OK;
 }
 
@@ -431,6 +447,7 @@ int skinny_gemm_ex(const void *x, const void *W, const void *residual, void *y, 
     DevState *d = nullptr;
     int rc = device_state(&d);
     if (rc) return rc;
+    if ((rc = refuse_after_give_up(d->err_host))) return rc;
     kp_cfg c;
     if (cfg && cfg->kind != KP_KIND_AUTO) {
         c = *cfg;
@@ -513,6 +530,7 @@ int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_plan **
     cudaGetDevice(&p->dev);
     p->sms = d->sms;
     p->err = d->err;
+    p->err_host = d->err_host;
     p->overlap.assign(max_M + 1, 1);
     Scratch need[3];
     for (int b = 0; b < 3; ++b) {
@@ -612,6 +630,8 @@ int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, cons
     if (dev != plan->dev)
         return set_error(KP_EINVAL, "kda_proj_run: current device %d is not the plan's device %d",
                          dev, plan->dev);
+    int rc = refuse_after_give_up(plan->err_host);
+    if (rc) return rc;
 
     const int mode = kda_proj_overlap_at(plan, M);
     const bool overlap = mode == 1 && aux_stream && events && events[0] && events[1];

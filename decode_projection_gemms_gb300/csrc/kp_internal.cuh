@@ -23,7 +23,7 @@ struct GemmArgs {
     int M, N, K;
     float *ws;               // split-K partials (may be null if unused)
     int *counters;           // per-tile tickets, zero between launches
-    int *err;                // device error word
+    int *err;                // error word (mapped host memory, device view)
     // Element type of x, W, y and the residual (KP_BF16 or KP_FP16; the
     // pointers above are raw 16-bit storage), and an optional residual
     // [M, ldr] added to the fp32 sum before the one rounding.
@@ -210,7 +210,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
-            if (err) atomicCAS(err, 0, code);
+            if (err) atomicCAS_system(err, 0, code);   // host-mapped word
             return false;
         }
     }

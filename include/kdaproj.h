@@ -35,8 +35,13 @@
  * kp_status otherwise, and kp_last_error() (thread-local) then describes the
  * failure, including the CUDA runtime's message for KP_ECUDA. Argument errors
  * are detected before anything is enqueued. Nothing throws across this ABI.
- * Kernel-side waits are bounded: a wait that runs out records a code that
- * kp_device_error() returns, and the kernel finishes instead of hanging.
+ * Kernel-side waits are bounded: a wait that runs out (after about 1 s, e.g.
+ * on a GPU that is pre-empted or time-sliced away) records a code in the
+ * device's error word and the kernel finishes instead of hanging. The outputs
+ * of that call are then undefined. The word lives in mapped host memory, so
+ * skinny_gemm, skinny_gemm_ex and kda_proj_run check it on entry without any
+ * CUDA call and return KP_EDEVICE while it is set; kp_device_error() reads
+ * and clears it.
  *
  * Determinism: the configuration used for a call depends only on (M, N, K)
  * and the loaded table (never on stream state), and every split-K reduction
@@ -75,7 +80,10 @@ enum kp_status {
     KP_ETOOBIG = -6,  /* M above the plan's max_M (its workspace would overflow) */
     KP_ENODEV = -7,   /* current device is not an sm_103 GPU */
     KP_ECONFIG = -8,  /* explicit kp_cfg invalid for this shape */
-    KP_EIO = -9       /* autotune table file unreadable or malformed */
+    KP_EIO = -9,      /* autotune table file unreadable or malformed */
+    KP_EDEVICE = -10  /* an earlier kernel wait on this device ran out (its
+                         outputs are undefined); nothing was enqueued.
+                         kp_device_error() returns the code and clears it */
 };
 
 /* Kernel families. */
@@ -96,7 +104,14 @@ enum kp_flags {
     KP_FLAG_PDL = 1,    /* launch with programmatic stream serialisation: the
                            kernel may start (and stream its weights) while the
                            previous kernel on the stream finishes; it waits for
-                           that kernel before touching x, y or scratch */
+                           that kernel before touching x, y, the residual or
+                           scratch. W (and the projection's W_fb) is read
+                           BEFORE that wait, so W must not be written by the
+                           kernel just before on the same stream (weights
+                           never are; this library's kernels let their
+                           dependents start before they store y, so feeding
+                           one call's y as the next call's W needs a
+                           configuration without this flag) */
     KP_FLAG_FUSE_FB = 2 /* F_A/beta branch of kda_proj_run only (TC05 kind,
                            M <= 256): the F_A/beta launch also computes F_B
                            from its bf16 F_A tile, so the F_B launch is skipped */
@@ -162,7 +177,7 @@ KP_API int skinny_gemm(const void *x, const void *W, void *y, int M, int N, int 
  * table is keyed by shape only). skinny_gemm(x, W, y, ...) is
  * skinny_gemm_ex(x, W, NULL, y, ..., KP_BF16, ...).
  * Returns KP_OK, KP_EINVAL (also for an unknown dtype), KP_EALIGN, KP_ESHAPE,
- * KP_ECONFIG, KP_ENODEV, KP_ECUDA. */
+ * KP_ECONFIG, KP_ENODEV, KP_ECUDA, KP_EDEVICE. */
 KP_API int skinny_gemm_ex(const void *x, const void *W, const void *residual, void *y, int M,
                           int N, int K, int dtype, const kp_cfg *cfg, kp_stream_t stream);
 
@@ -191,15 +206,27 @@ KP_API int kp_table_size(void);
  * synchronisation. The caller still passes x, W and y (same layout as
  * skinny_gemm); the call calls no cudaMalloc, cudaFree or allocating library
  * routine.
- *   - Limits: M <= 16 (CUDA-core kernel); the split-K partial sums
- *     (split_k * M * N floats) must fit in KP_NOALLOC_SCRATCH_FLOATS and the
- *     row tiles in KP_NOALLOC_TICKETS; larger needs return KP_ETOOBIG. With
- *     cfg NULL (or kind AUTO) a CUDA-core configuration that fits is chosen;
- *     an explicit cfg must be kind KP_KIND_CC.
+ *   - Limits: M <= 16 (CUDA-core kernel). The kernel stages x's K slice in
+ *     shared memory (M * ceil(K / split_k) * 4 bytes, at most 200 KiB), so a
+ *     shape needs split_k >= ceil(M * K * 4 / 204800); its split-K partial
+ *     sums (split_k * M * N floats when split_k > 1) must fit in
+ *     KP_NOALLOC_SCRATCH_FLOATS and its row tiles (ceil(N / 32) with the
+ *     default configuration) in KP_NOALLOC_TICKETS. With cfg NULL (or kind
+ *     AUTO) the entry point sizes split_k for about two CTAs per SM, lowers
+ *     it until the partial sums fit, then raises it again if x's slice does
+ *     not fit in shared memory; a shape whose smallest such split_k needs
+ *     more partial sums than the array holds (e.g. M = 16, K = 16384,
+ *     N = 8192: split_k >= 6, 786432 floats) returns KP_ETOOBIG. An explicit
+ *     cfg must be kind KP_KIND_CC.
+ *   - Ordering: with cfg NULL the kernel launches without programmatic
+ *     dependent launch, so x and W may both come from the kernel just before
+ *     it on the stream. A cfg (kind AUTO or CC) supplies the flags, and with
+ *     KP_FLAG_PDL W is read before that wait (see KP_FLAG_PDL).
  *   - Memory: every GPU that loads the library holds the array
  *     (2 MiB + 32 KiB) until the process exits.
- *   - First call per device: looks up the array's device address and zeroes
- *     its tickets (synchronises that device); make it before any stream
+ *   - First call per device: looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); it allocates and
+ *     synchronises nothing, but make that first call before any stream
  *     capture. Later calls only launch the kernel.
  *   - Sharing: all calls on a device use the same array and it keeps the last
  *     call's partial sums; calls that overlap on the GPU (different streams,
@@ -278,12 +305,14 @@ KP_API int kda_proj_destroy(kda_plan *plan);
  * Diagnostics. */
 KP_API const char *kp_last_error(void);           /* thread-local, never NULL */
 KP_API int kp_version(void);                       /* KDAPROJ_VERSION */
-/* Reads and clears the device-side error word of the current device: 0 if
- * no kernel wait has run out, else the code of the first one: 1 a stage of
- * operands never landed, 2 a pipeline stage was never freed, 3 an
- * accumulator was never ready, 4 an accumulator was never drained, 5 the
- * self-test below (synchronous: it waits for the device).
- * Returns KP_OK or KP_ECUDA. */
+/* Reads and clears (one atomic exchange, no CUDA call) the error word of the
+ * current device: 0 if no kernel wait has run out, else the code of the
+ * first one since the last read: 1 a stage of operands never landed, 2 a
+ * pipeline stage was never freed, 3 an accumulator was never ready, 4 an
+ * accumulator was never drained, 5 the self-test below. It does not wait for
+ * the device: a kernel still running may set the word later, so read it once
+ * the work in question has completed (e.g. after cudaStreamSynchronize).
+ * Returns KP_OK, KP_ENODEV or KP_ECUDA. */
 KP_API int kp_device_error(int *code);
 /* Self-test of the failure path: launches one CTA on `stream` that waits on a
  * barrier nothing completes, with the kernels' bounded wait cut to timeout_us

@@ -36,6 +36,38 @@ def test_wait_runs_out_and_reports():
     assert binding.device_error() == 0
 
 
+def test_give_up_is_refused_until_read():
+    """After a wait ran out, the entry points refuse new work (KP_EDEVICE, a
+    host-visible error without a synchronising call) until kp_device_error()
+    has read and cleared the code; then they run again."""
+    binding.selftest_timeout(1000)
+    torch.cuda.synchronize()
+    x, W = gemm_case(2, 264, 1024, seed=3)
+    x, W = x.cuda(), W.cuda()
+    with pytest.raises(binding.KdaProjError) as e:
+        binding.skinny_gemm(x, W)
+    assert e.value.code == binding.KP_EDEVICE
+    plan = binding.KdaPlan(K=1024, N_qkvg=256, N_fab=136, N_fb=64, max_M=4)
+    try:
+        wp = torch.zeros((392, 1024), dtype=torch.bfloat16, device="cuda")
+        wfb = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(binding.KdaProjError) as e:
+            plan.run(x, wp, wfb)
+        assert e.value.code == binding.KP_EDEVICE
+        assert binding.device_error() == binding.DEV_SELFTEST
+        plan.run(x, wp, wfb)                  # accepted again
+        torch.cuda.synchronize()
+    finally:
+        plan.close()
+    check_gemm(x.cpu(), W.cpu(), None, "after reading the code")
+    # the binding's checked run raises on a give-up during the call itself
+    binding.selftest_timeout(1000)
+    with pytest.raises(binding.KdaProjError) as e:
+        binding.check_device()
+    assert e.value.code == binding.KP_EDEVICE
+    assert binding.device_error() == 0
+
+
 def test_first_code_wins_and_streams_keep_order():
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
