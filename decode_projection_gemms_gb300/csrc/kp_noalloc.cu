@@ -12,8 +12,10 @@
 // library holds it (KP_NOALLOC_SCRATCH_FLOATS floats + KP_NOALLOC_TICKETS
 // ints) until the process exits. Host code may not use the array's name as a
 // device address, so the first call on each device looks the address up with
-// cudaGetSymbolAddress (with that device current) and zeroes the tickets;
-// later calls reuse the cached address.
+// cudaGetSymbolAddress (with that device current); later calls reuse the
+// cached address. The tickets start at zero (a __device__ array is
+// zero-initialised when the module loads) and every launch leaves them at
+// zero, so nothing is cleared at set-up and no call synchronises.
 #include <cstring>
 #include <mutex>
 
@@ -42,8 +44,8 @@ int cuda_fail(cudaError_t e, const char *what) {
 }
 
 // Once per device, with that device current: resolve the arrays' device
-// addresses and clear the tickets (the kernel leaves them at zero after every
-// completed launch).
+// addresses. The tickets need no clearing: zero at module load, and the last
+// CTA of every row tile resets its ticket before it exits.
 int setup(NoAllocState **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -68,9 +70,6 @@ int setup(NoAllocState **out) {
         if ((e = cudaGetSymbolAddress(&p, g_noalloc_tickets)) != cudaSuccess)
             return cuda_fail(e, "cudaGetSymbolAddress(tickets)");
         s.tickets = static_cast<int *>(p);
-        if ((e = cudaMemset(s.tickets, 0, sizeof(int) * KP_NOALLOC_TICKETS)) != cudaSuccess)
-            return cuda_fail(e, "clearing the tickets");
-        if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
         s.ready = true;
     }
     *out = &s;
@@ -79,7 +78,9 @@ int setup(NoAllocState **out) {
 
 // Default CUDA-core configuration that fits the fixed scratch: about two CTAs
 // per SM, fewer K slices when the partial sums would not fit (one slice needs
-// no scratch at all).
+// no scratch at all). No programmatic dependent launch: the kernel would read
+// W before waiting for the previous kernel on the stream, and a caller of
+// this entry point may have just computed W there.
 kp_cfg default_cfg(int M, int N, int K, int sms) {
     kp_cfg c;
     memset(&c, 0, sizeof c);
@@ -87,7 +88,7 @@ kp_cfg default_cfg(int M, int N, int K, int sms) {
     c.block = 256;
     c.rows = 4;
     c.k_unroll = 2;
-    c.flags = KP_FLAG_PDL;
+    c.flags = 0;
     const int rows_cta = 8 * c.rows;
     const int tiles = (N + rows_cta - 1) / rows_cta;
     int S = (2 * sms + tiles - 1) / tiles;

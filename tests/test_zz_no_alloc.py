@@ -77,7 +77,34 @@ def test_noalloc_rejects_what_does_not_fit(lib):
     too_many_slices = KpCfg.make("cc", split_k=28, block=256, rows=4, k_unroll=1)
     assert _noalloc(lib, x, W, y, too_many_slices) == binding.KP_ETOOBIG
     assert b"fixed scratch" in lib.kp_last_error()
+    # the entry point's own choice cannot fit either: x's slice needs
+    # split_k >= 6 at K = 16384, and 6 * 16 * 8192 partial sums exceed the array
+    xk = gen_x(16, 16384, seed=4).cuda()
+    Wk = torch.zeros((8192, 16384), dtype=torch.bfloat16, device="cuda")
+    yk = torch.empty((16, 8192), dtype=torch.bfloat16, device="cuda")
+    assert _noalloc(lib, xk, Wk, yk, None) == binding.KP_ETOOBIG
+    del Wk
     x17 = gen_x(17, 7168, seed=3).cuda()
     y17 = torch.empty((17, 8192), dtype=torch.bfloat16, device="cuda")
     assert _noalloc(lib, x17, W, y17, None) == binding.KP_ECONFIG
     assert _noalloc(lib, x, W, y, KpCfg.make("tc05", split_k=4)) == binding.KP_ECONFIG
+
+
+def test_noalloc_reads_a_w_written_by_the_kernel_before_it(lib):
+    """With cfg NULL there is no programmatic dependent launch: a W that the
+    previous kernel on the stream (here skinny_gemm, whose kernels let their
+    dependents start before they store) has just written is read complete."""
+    M, K1, N1 = 8, 2048, 1024   # first call: T = bf16(x1 @ W1^T), [8, 1024]
+    x1 = gen_x(M, K1, seed=51).cuda()
+    W1 = gen_w(N1, K1, seed=52, std=0.5).cuda()
+    x2 = gen_x(4, N1, seed=53).cuda()   # second call: y = bf16(x2 @ T^T), W = T
+    for _ in range(2):
+        T = torch.full((M, N1), float("nan"), dtype=torch.bfloat16, device="cuda")
+        y = torch.full((4, M), float("nan"), dtype=torch.bfloat16, device="cuda")
+        binding.skinny_gemm(x1, W1, T)                       # the table's choice, with PDL
+        rc = _noalloc(lib, x2, T, y, None)
+        assert rc == binding.KP_OK, lib.kp_last_error().decode()
+        torch.cuda.synchronize()
+        ref = oracle.gemm(bf16_bits(x2.cpu()), bf16_bits(T.cpu()))
+        r = oracle.compare(y.float().cpu().numpy().astype(np.float64), ref)
+        assert r["ok"], r
