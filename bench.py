@@ -45,6 +45,38 @@ WORKLOAD = ("full KDA decode projection: packed [4096+136, 7168] bf16 + W_fb [10
             "graph-replayed, 48-layer weight stack rotated per call")
 
 
+# ncu DRAM traffic of the single-launch projection kernel per token count (a
+# profiles/ summary); used only while the kernel's sources are unchanged since
+# that capture (their hash is recorded in it)
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "tc05_single_n4232_k7168_dram_by_m.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "decode_projection_gemms_gb300", "csrc", f)
+                  for f in ("kp_tc05.cu", "kp_internal.cuh")]
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """{M: DRAM bytes read + written per launch} from the summary, or None if
+    it is missing or was taken on other kernel sources."""
+    try:
+        text = open(TRAFFIC_SUMMARY).read()
+    except OSError:
+        return None, "no ncu summary"
+    import re
+    m = re.search(r"kernel sources sha256\[:16\]: `?([0-9a-f]{16})", text)
+    if not m or m.group(1) != kernel_source_hash():
+        return None, "kernel sources changed since the ncu capture"
+    rows = re.findall(r"^\|\s*(\d+)\s*\|\s*([\d.]+)\s*\|\s*([\d.]+)\s*\|", text, re.M)
+    return {int(M): float(r) + float(w) for M, r, w in rows}, "ncu capture, " + os.path.relpath(
+        TRAFFIC_SUMMARY, ROOT)
+
+
 def call_bytes(M: int) -> int:
     """Algorithmic bytes of one projection call: 2(MK + NK + MN) per GEMM."""
     g = lambda m, n, k: 2 * (m * k + n * k + m * n)
@@ -338,7 +370,48 @@ def run_ours(args):
         for Ms, row in cc["per_m"].items():
             if Ms in per_m:   # the tcgen05 kernel on the same shape, same run
                 row["tcgen05_us"] = per_m[Ms]["qkvg_kernel_us"]
-    achieved = q_bytes / (q_time_us * 1e3)  # GB/s
+    q_achieved = q_bytes / (q_time_us * 1e3)  # GB/s
+    # The timed mode's dominant kernel: the single-launch projection where the
+    # table picks it (one kernel per call), else the Q/K/V/G GEMM.
+    for M in keys:
+        row = per_m[str(M)]
+        if plan.overlap_at(M) == 2:
+            row["timed_kernel"] = {"kernel": "single-launch projection", "us": row["us_single_launch"],
+                                   "gbs": round(call_bytes(M) / (row["us_single_launch"] * 1e3), 1)}
+        else:
+            row["timed_kernel"] = {"kernel": "Q/K/V/G GEMM", "us": row["qkvg_kernel_us"],
+                                   "gbs": row["qkvg_kernel_gbs"]}
+        row["timed_kernel"]["frac_of_hbm"] = round(row["timed_kernel"]["gbs"] / hbm_peak, 4)
+    one = [M for M in keys if plan.overlap_at(M) == 2]
+    traffic, traffic_src = load_traffic()
+    if one:
+        o_bytes = sum(call_bytes(M) for M in one)
+        o_time = sum(per_m[str(M)]["us_single_launch"] for M in one)
+        tr = None
+        if traffic is not None and all(M in traffic for M in one):
+            tr = round(statistics.fmean(traffic[M] for M in one))
+        roofline = {"bound": "hbm", "achieved": round(o_bytes / (o_time * 1e3), 1), "peak": hbm_peak,
+                    "unit": "GB/s", "frac": round(o_bytes / (o_time * 1e3) / hbm_peak, 4),
+                    "traffic": tr,
+                    "algorithmic_bytes_per_launch": round(o_bytes / len(one)),
+                    "traffic_source": traffic_src if tr is not None else
+                    f"null: {traffic_src if traffic is None else 'capture lacks some M'}",
+                    "kernel": "single-launch projection (tcgen05, packed [4232, 7168] weight, "
+                              "fused F_B), the timed mode's only kernel",
+                    "M": one,
+                    "units": "achieved = sum over these M of 2(MK+NK+MN) bytes of the three GEMMs / "
+                             "sum of per-launch device time; traffic = mean DRAM read+write "
+                             "bytes per launch over the same M",
+                    "peak_source": f"{peak_src} hbm_gbs (copy bandwidth, burst)"}
+    else:
+        roofline = {"bound": "hbm", "achieved": round(q_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(q_achieved / hbm_peak, 4), "traffic": None,
+                    "kernel": "Q/K/V/G GEMM", "peak_source": f"{peak_src} hbm_gbs"}
+    roofline_qkvg = {"achieved": round(q_achieved, 1), "unit": "GB/s",
+                     "frac": round(q_achieved / hbm_peak, 4), "M": keys,
+                     "kernel": "Q/K/V/G GEMM (per-M configured kernel), timed alone"}
+    eager = None if args.no_extras else run_eager(args, plan, wp_stack, wfb_stack, xs, outs, main,
+                                                  aux, evs, dist)
     n_launches = args.steps * L * sum(launches_per_call(M) for M in keys)
     cpu = run_cpu_baseline(args, m_list) if (rank == 0 and not args.no_cpu) else None
     plan.close()
@@ -364,11 +437,8 @@ def run_ours(args):
                        "value_is": "mean over M of device time per projection call",
                        "parallelism": f"replicas x{ws}"},
             "per_m": per_m,
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1),
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(achieved / hbm_peak, 4), "traffic": None,
-                         "kernel": "Q/K/V/G GEMM (per-M configured kernel), timed alone",
-                         "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"},
+            "roofline": roofline,
+            "roofline_qkvg_alone": roofline_qkvg,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": n_launches,
@@ -376,6 +446,7 @@ def run_ours(args):
             "cuda_core_splitk": cc,
             "prefill": prefill,
             "pdl_handoff": handoff,
+            "eager": eager,
             "clocks": clock_info,
         }
         print(json.dumps(line))
@@ -579,6 +650,59 @@ def run_handoff(args, plan, wp_stack, wfb_stack, xs, outs, dev, main, aux, evs, 
     return out
 
 
+def run_eager(args, plan, wp_stack, wfb_stack, xs, outs, main, aux, evs, dist, m_e=(1, 16, 128)):
+    """The projection called eagerly (no graph): host time per call to enqueue
+    it, through the Python binding and through the bare C ABI (ctypes with
+    prepared arguments), and the device time per call of the eager chain of
+    48 calls (one layer each)."""
+    import ctypes
+    import torch
+    from decode_projection_gemms_gb300 import binding
+    L = args.layers
+    lib = binding.load()
+    out = {"calls_per_sample": L, "per_m": {}}
+    for M in m_e:
+        if M not in xs:
+            continue
+        oq, of, ob = outs[M]
+        ms = ctypes.c_void_p(int(main.cuda_stream))
+        ax = ctypes.c_void_p(int(aux.cuda_stream))
+        ev = (ctypes.c_void_p * 2)(int(evs[0].cuda_event), int(evs[1].cuda_event))
+        h = ctypes.c_void_p(plan.handle)
+        raw = [(h, ctypes.c_void_p(xs[M].data_ptr()), ctypes.c_void_p(wp_stack[layer].data_ptr()),
+                ctypes.c_void_p(wfb_stack[layer].data_ptr()), ctypes.c_void_p(oq.data_ptr()),
+                ctypes.c_void_p(of.data_ptr()), ctypes.c_void_p(ob.data_ptr()), M, ms, ax, ev)
+               for layer in range(L)]
+        host_py, host_c, dev_us = [], [], []
+        with torch.cuda.stream(main):
+            for rep in range(6):
+                torch.cuda.synchronize()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(main)
+                t0 = time.perf_counter()
+                if rep % 2 == 0:
+                    for layer in range(L):
+                        plan.run(xs[M], wp_stack[layer], wfb_stack[layer], oq, of, ob,
+                                 aux_stream=aux, events=evs)
+                else:
+                    for r in raw:
+                        if lib.kda_proj_run(*r) != 0:
+                            raise binding.KdaProjError(-5, binding.last_error())
+                t1 = time.perf_counter()
+                b.record(main)
+                torch.cuda.synchronize()
+                if rep >= 2:   # the first pair warms up
+                    (host_py if rep % 2 == 0 else host_c).append((t1 - t0) * 1e6 / L)
+                    dev_us.append(a.elapsed_time(b) * 1e3 / L)
+        vals = reduce_max([statistics.median(host_py), statistics.median(host_c),
+                           statistics.median(dev_us)], dist)
+        out["per_m"][str(M)] = {"host_us_per_call_binding": round(vals[0], 2),
+                                "host_us_per_call_c_abi": round(vals[1], 2),
+                                "device_us_per_call_eager": round(vals[2], 3)}
+    return out
+
+
 def run_e2e(args, plan, wp_stack, wfb_stack, m_list, dev, main, aux, evs, dist):
     """Same metric through the public API with host buffers: every call has
     its own x in pinned host memory and its own output block (the three
@@ -702,14 +826,42 @@ def oracle_step(stride: int, nthreads: int, m_list):
     return statistics.fmean(times)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        fields = dict(line.split(":", 1) for line in out.splitlines() if ":" in line)
+        fields = {k.strip(): v.strip() for k, v in fields.items()}
+        name = fields.get("Model name")
+        if name:
+            vendor = fields.get("Vendor ID")
+            return f"{vendor} {name}" if vendor and vendor not in name else name
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def run_cpu_baseline(args, m_list):
+    """The oracle on the host: all cores over output features (all columns),
+    and one thread on a column sample (every 16th feature, scaled up)."""
     nthreads = os.cpu_count() or 1
-    stride = 1
-    t = oracle_step(stride, nthreads, m_list)
+    t = oracle_step(1, nthreads, m_list)
+    t1 = oracle_step(16, 1, m_list)
     return {"value": round(t * 1e6, 1), "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"double-precision oracle, full projection (all output features), one "
                       f"call per M in {list(m_list)} on layer 0, {nthreads} threads over output "
-                      f"features; mean over M"}
+                      f"features; mean over M",
+            "single_thread": {"value": round(t1 * 1e6, 1), "unit": UNIT, "cores": 1,
+                              "sample": "one thread, every 16th output feature of Q/K/V/G and "
+                                        "F_B (all of F_A/beta), scaled to all features; mean "
+                                        "over the same M values"}}
 
 
 def run_reference(args):
@@ -736,7 +888,7 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "M": m_list, "K": K, "N_qkvg": N_QKVG, "N_fab": N_FAB,
                    "N_fb": N_FB, "value_is": "mean over M of host time per projection call"},
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": nthreads,
-                         "kind": "oracle",
+                         "kind": "oracle", "cpu_model": cpu_model(),
                          "sample": f"every {args.cpu_stride}th output feature of Q/K/V/G and F_B, "
                                    "all of F_A/beta, scaled to all columns"},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
