@@ -40,8 +40,8 @@
 // x + j*Mpad*128.
 // TMEM: one fp32 accumulator of Mpad columns, lane = feature row.
 #include <cstring>
+#include <map>
 #include <mutex>
-#include <set>
 #include <type_traits>
 #include <utility>
 
@@ -174,12 +174,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     // The fused F_B tile (if any) is dispatched first: its cluster has the
     // longest epilogue.
-    const int tile = (static_cast<int>(blockIdx.x) / C + p.tile_rot) % p.n_tiles;
+    int tile = (static_cast<int>(blockIdx.x) / C + p.tile_rot) % p.n_tiles;
+    // Token tile of this CTA: tokens [m0, m0 + Mloc). Blocks are dispatched
+    // in linear order (x fastest); without clusters the linear id is remapped
+    // so that the token tiles of one feature tile are consecutive: they run in
+    // the same wave and all but the first read the tile's weights from L2
+    // (with feature tiles fastest, a grid larger than one wave re-streamed
+    // every weight tile from HBM in the next wave).
+    int ttile = static_cast<int>(blockIdx.y);
+    if (kTiled && C == 1) {
+        const int id = static_cast<int>(blockIdx.x + blockIdx.y * gridDim.x);
+        ttile = id % static_cast<int>(gridDim.y);
+        tile = id / static_cast<int>(gridDim.y);
+    }
     const bool fused = (p.fb_tile >= 0 && tile == p.fb_tile);
-    // Token tile of this CTA: tokens [m0, m0 + Mloc). All token tiles of a
-    // feature tile run together, so its weights come from HBM once and from
-    // L2 for the other token tiles.
-    const int m0 = kTiled ? static_cast<int>(blockIdx.y) * p.Mpad : 0;
+    const int m0 = kTiled ? ttile * p.Mpad : 0;
     const int Mloc = kTiled ? min(p.M - m0, p.Mpad) : p.M;
     const int kb0 = static_cast<int>((static_cast<long long>(p.KB) * rank) / C);
     const int kb1 = static_cast<int>((static_cast<long long>(p.KB) * (rank + 1)) / C);
@@ -603,7 +612,13 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
-std::set<int> g_attr_devices;
+// Per device: kernel attributes raised, and the SM's shared memory and the
+// per-block reserve (read once, used by every launch's TMEM-safety padding).
+struct DevAttrs {
+    int sm_smem = 0;
+    int reserved = 0;
+};
+std::map<int, DevAttrs> g_attr_devices;
 
 cudaError_t get_encode(EncodeTiledFn *out) {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -620,6 +635,53 @@ cudaError_t get_encode(EncodeTiledFn *out) {
     return cudaSuccess;
 }
 
+// Encoded tensor maps, cached. A map is a pure function of (address, shape,
+// row stride, box, element type), all of which form the key, so a cached copy
+// is always the map the encoder would return: an address that is freed and
+// reused for another tensor of the same shape gets the same, correct map.
+// Direct-mapped, 1024 slots; a colliding key replaces the slot.
+struct MapKey {
+    const void *ptr;
+    int64_t ld;
+    int rows, cols, box_rows, nkb, dtype, rank;
+    bool operator==(const MapKey &o) const {
+        return ptr == o.ptr && ld == o.ld && rows == o.rows && cols == o.cols &&
+               box_rows == o.box_rows && nkb == o.nkb && dtype == o.dtype && rank == o.rank;
+    }
+};
+struct MapSlot {
+    bool valid = false;
+    MapKey key;
+    CUtensorMap map;
+};
+constexpr int kMapSlots = 1024;
+std::mutex g_map_mu;
+MapSlot g_maps[kMapSlots];
+
+int map_slot(const MapKey &k) {
+    uint64_t h = reinterpret_cast<uint64_t>(k.ptr) * 0x9E3779B97F4A7C15ull;
+    for (int64_t v : {k.ld, static_cast<int64_t>(k.rows), static_cast<int64_t>(k.cols),
+                      static_cast<int64_t>(k.box_rows) * 64 + k.nkb * 4 + k.dtype * 2 + k.rank})
+        h = (h ^ static_cast<uint64_t>(v)) * 0x100000001B3ull;
+    return static_cast<int>((h >> 32) % kMapSlots);
+}
+
+bool map_lookup(const MapKey &k, CUtensorMap *out) {
+    const int i = map_slot(k);
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (!g_maps[i].valid || !(g_maps[i].key == k)) return false;
+    memcpy(out, &g_maps[i].map, sizeof(CUtensorMap));
+    return true;
+}
+
+void map_store(const MapKey &k, const CUtensorMap &m) {
+    const int i = map_slot(k);
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_maps[i].valid = true;
+    g_maps[i].key = k;
+    memcpy(&g_maps[i].map, &m, sizeof(CUtensorMap));
+}
+
 // 2-D bf16 tensor map: `rows` x `cols` (cols contiguous, row stride `ld`
 // elements), box = box_rows x 64 columns, 128-byte swizzle, zero fill.
 CUtensorMapDataType map_type(int dtype) {
@@ -628,6 +690,8 @@ CUtensorMapDataType map_type(int dtype) {
 
 cudaError_t make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int64_t ld,
                      int box_rows, int dtype = KP_BF16) {
+    const MapKey key{ptr, ld, rows, cols, box_rows, 0, dtype, 2};
+    if (map_lookup(key, map)) return cudaSuccess;
     EncodeTiledFn enc;
     cudaError_t e = get_encode(&enc);
     if (e != cudaSuccess) return e;
@@ -639,7 +703,9 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int6
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    map_store(key, *map);
+    return cudaSuccess;
 }
 
 // 3-D bf16 view of a [rows, cols] row-major matrix as (64, rows, cols / 64):
@@ -647,6 +713,8 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int rows, int cols, int6
 // one copy lands nkb consecutive [box_rows][64] blocks. Needs cols % 64 == 0.
 cudaError_t make_map3(CUtensorMap *map, const void *ptr, int rows, int cols, int64_t ld,
                       int box_rows, int nkb, int dtype) {
+    const MapKey key{ptr, ld, rows, cols, box_rows, nkb, dtype, 3};
+    if (map_lookup(key, map)) return cudaSuccess;
     EncodeTiledFn enc;
     cudaError_t e = get_encode(&enc);
     if (e != cudaSuccess) return e;
@@ -660,7 +728,9 @@ cudaError_t make_map3(CUtensorMap *map, const void *ptr, int rows, int cols, int
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    map_store(key, *map);
+    return cudaSuccess;
 }
 
 // Tokens per CTA (the MMA's N): M padded to 16, at most 256 (one token tile).
@@ -879,9 +949,13 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    DevAttrs da;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_attr_devices.count(dev)) {
+        auto it = g_attr_devices.find(dev);
+        if (it != g_attr_devices.end()) {
+            da = it->second;
+        } else {
             for (auto fn : {tc05_kernel<false, false, false>, tc05_kernel<true, false, false>,
                             tc05_kernel<false, true, false>, tc05_kernel<true, true, false>,
                             tc05_kernel<false, false, true>, tc05_kernel<true, false, true>,
@@ -892,7 +966,10 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
                     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
             }
             if (e != cudaSuccess) return e;
-            g_attr_devices.insert(dev);
+            if (cudaDeviceGetAttribute(&da.sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&da.reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+                return cudaErrorInvalidValue;
+            g_attr_devices[dev] = da;
         }
     }
 
@@ -908,12 +985,8 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
     size_t smem = smem_of(Mpad, nkb, stages, rt);
     {
         const uint32_t cols = p.tmem_cols_fb > p.tmem_cols ? p.tmem_cols_fb : p.tmem_cols;
-        int sm_smem = 0, reserved = 0;
-        if (cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
-            return cudaErrorInvalidValue;
         const long long need =
-            (static_cast<long long>(sm_smem) * cols + 511) / 512 - reserved;
+            (static_cast<long long>(da.sm_smem) * cols + 511) / 512 - da.reserved;
         if (need > static_cast<long long>(smem)) smem = static_cast<size_t>(need);
         if (smem > static_cast<size_t>(kMaxSmem)) return cudaErrorInvalidValue;
     }
