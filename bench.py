@@ -45,12 +45,12 @@ WORKLOAD = ("full KDA decode projection: packed [4096+136, 7168] bf16 + W_fb [10
             "graph-replayed, 48-layer weight stack rotated per call")
 
 
-# ncu DRAM traffic of the single-launch projection kernel per token count (a
-# profiles/ summary); used only while the kernel's sources are unchanged since
+# ncu DRAM traffic of the single-launch projection kernels per token count (a
+# profiles/ summary); used only while the kernels' sources are unchanged since
 # that capture (their hash is recorded in it)
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "tc05_single_n4232_k7168_dram_by_m.md")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "single_launch_n4232_k7168_dram_by_m.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "decode_projection_gemms_gb300", "csrc", f)
-                  for f in ("kp_tc05.cu", "kp_internal.cuh")]
+                  for f in ("kp_tc05.cu", "kp_cc_kernel.cuh", "kp_internal.cuh")]
 
 
 def kernel_source_hash() -> str:
@@ -376,7 +376,9 @@ def run_ours(args):
     for M in keys:
         row = per_m[str(M)]
         if plan.overlap_at(M) == 2:
-            row["timed_kernel"] = {"kernel": "single-launch projection", "us": row["us_single_launch"],
+            kind = binding.KIND_NAMES[plan.get_config(binding.BRANCH_QKVG, M).kind]
+            row["timed_kernel"] = {"kernel": f"single-launch projection ({kind})",
+                                   "us": row["us_single_launch"],
                                    "gbs": round(call_bytes(M) / (row["us_single_launch"] * 1e3), 1)}
         else:
             row["timed_kernel"] = {"kernel": "Q/K/V/G GEMM", "us": row["qkvg_kernel_us"],
@@ -396,8 +398,11 @@ def run_ours(args):
                     "algorithmic_bytes_per_launch": round(o_bytes / len(one)),
                     "traffic_source": traffic_src if tr is not None else
                     f"null: {traffic_src if traffic is None else 'capture lacks some M'}",
-                    "kernel": "single-launch projection (tcgen05, packed [4232, 7168] weight, "
-                              "fused F_B), the timed mode's only kernel",
+                    "kernel": "single-launch projection over the packed [4232, 7168] weight with "
+                              "F_B fused (the timed mode's only kernel per call): CUDA-core at M "
+                              f"{[M for M in one if plan.get_config(0, M).kind == binding.KIND_CC]}, "
+                              "tcgen05 at M "
+                              f"{[M for M in one if plan.get_config(0, M).kind == binding.KIND_TC05]}",
                     "M": one,
                     "units": "achieved = sum over these M of 2(MK+NK+MN) bytes of the three GEMMs / "
                              "sum of per-launch device time; traffic = mean DRAM read+write "

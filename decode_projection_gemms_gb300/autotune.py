@@ -39,7 +39,7 @@ SWEEP_K = [128, 1024, 7168, 16384]
 def cc_candidates(M: int, N: int, K: int, sms: int):
     out = []
     for (R, U) in ((1, 4), (2, 2), (2, 4), (4, 1), (4, 2), (8, 1)):
-        for block in (128, 256):
+        for block in (128, 256, 512):
             rows_cta = (block // 32) * R
             tiles = math.ceil(N / rows_cta)
             for waves in (1, 2, 4, 8):
@@ -63,7 +63,9 @@ def tc05_candidates(M: int, N: int, K: int, sms: int):
             if T * C > 2 * sms:
                 continue
             for nkb in (1, 2, 4):
-                for P in sorted({1, min(nkb, 2), nkb}):
+                # more producer warps where one CTA per SM streams W and x
+                ps = {1, min(nkb, 2), nkb} | ({3, 5} if M >= 32 and nkb >= 2 else set())
+                for P in sorted(ps):
                     for stages in (0, 2, 3, 4):
                         out.append(KpCfg.make("tc05", split_k=C, rows=rows, k_unroll=nkb,
                                               producers=P, stages=stages))
@@ -297,10 +299,16 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
         pb.plan.set_config(binding.BRANCH_FB, M, cb)
         us_ovl = pb.time_call(M, 1)
         us_seq = pb.time_call(M, 0)
-        # single launch over the packed weight with the best tcgen05 configs
+        # single launch over the packed weight: the best tcgen05 configs, and at
+        # M <= 8 the CUDA-core kernel with one K slice (its F_A rows a cluster)
         us_one, c_one = None, None
-        for cand in [c for _, c in q_res if c.kind == binding.KIND_TC05] + tc05_candidates(
-                M, pb.Nq + pb.Nfab, pb.K, sms):
+        one_cands = [c for _, c in q_res if c.kind == binding.KIND_TC05] + tc05_candidates(
+            M, pb.Nq + pb.Nfab, pb.K, sms)
+        if M <= 8:
+            one_cands += [KpCfg.make("cc", split_k=1, block=b, rows=R, k_unroll=U)
+                          for (R, U) in ((1, 4), (2, 2), (2, 4), (4, 1), (4, 2))
+                          for b in (128, 256, 512) if (b // 32) * R <= 128]
+        for cand in one_cands:
             try:
                 pb.plan.set_config(binding.BRANCH_QKVG, M, cand)
             except binding.KdaProjError:
@@ -323,6 +331,30 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
         ov = min(times, key=times.get)
         if ov == 2:
             cq = c_one
+            # The table holds one Q/K/V/G configuration per M, which the
+            # two-stream mode then also runs: re-tune the aux branch for the
+            # overlapped mode beside it, so that mode is tuned as well.
+            pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
+            best_aux = None
+            for cf2 in f_cands:
+                for (_, cb2) in (b_res[:1] if cf2.flags & binding.FLAG_FUSE_FB else b_res):
+                    try:
+                        plain = KpCfg.from_buffer_copy(cf2)
+                        plain.flags &= ~binding.FLAG_FUSE_FB
+                        binding.scratch_bytes(M, pb.Nfab, pb.K, plain, sms)
+                        pb.plan.set_config(binding.BRANCH_FAB, M, cf2)
+                        pb.plan.set_config(binding.BRANCH_FB, M, cb2)
+                        us = pb.time_call(M, 1)
+                    except binding.KdaProjError:
+                        continue
+                    if best_aux is None or us < best_aux[0]:
+                        best_aux = (us, cf2, cb2)
+            if best_aux is not None:
+                _, cf, cb = best_aux
+                pb.plan.set_config(binding.BRANCH_FAB, M, cf)
+                pb.plan.set_config(binding.BRANCH_FB, M, cb)
+                times[1] = pb.time_call(M, 1, reps=30, trials=5)
+                us_ovl = times[1]
         pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
         lines += [table_line(M, pb.Nq, pb.K, cq, ov, times[ov]),
                   table_line(M, pb.Nfab, pb.K, cf, ov),

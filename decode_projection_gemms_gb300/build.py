@@ -25,6 +25,7 @@ SOURCES = [
     "kp_cc_inst_hi_bf16.cu",
     "kp_cc_inst_lo_fp16.cu",
     "kp_cc_inst_hi_fp16.cu",
+    "kp_cc_inst_proj.cu",
     "kp_tc05.cu",
     "kp_smallk.cu",
     "kp_noalloc.cu",

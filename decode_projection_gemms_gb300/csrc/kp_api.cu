@@ -237,9 +237,12 @@ struct BranchShape {
 static BranchShape branch_shape(const kda_plan *p, int b);
 
 // Whether the plan can run the whole projection as one launch at M with the
-// Q/K/V/G configuration c: tcgen05 kernel, F_A rows starting on a 128-row
-// tile, room for the fused F_B operands, no M slicing.
+// Q/K/V/G configuration c: the tcgen05 kernel (F_A rows starting on a 128-row
+// tile, room for the fused F_B operands, no M slicing), or the CUDA-core
+// kernel with one K slice (M <= 8, F_A rows a whole cluster of CTAs).
 static bool single_launch_ok(const kda_plan *p, int M, const kp_cfg &c) {
+    if (c.kind == KP_KIND_CC)
+        return p->Nfb >= 1 && cc_proj_supported(M, p->K, p->Nq + p->Nfab, c, p->Nq);
     return c.kind == KP_KIND_TC05 && M <= 256 && p->Nq % tc05_rows(c) == 0 &&
            tc05_supported(M, p->Nq + p->Nfab, p->K, c) && tc05_fusable(M, c);
 }
@@ -677,8 +680,9 @@ int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, cons
     cudaStream_t side = overlap ? static_cast<cudaStream_t>(aux_stream) : ms;
 
     if (mode == 2 && single_launch_ok(plan, M, cq)) {
-        // One tcgen05 launch over the packed weight: rows [0, N_qkvg) go to
-        // out_qkvg, the rest to out_fab, and the F_A tile's cluster computes
+        // One launch over the packed weight (tcgen05 or CUDA-core kernel, as
+        // the Q/K/V/G configuration says): rows [0, N_qkvg) go to out_qkvg,
+        // the rest to out_fab, and the cluster that owns the F_A rows computes
         // F_B. Q/K/V/G and F_A/beta tiles run side by side on the SMs.
         GemmArgs a = q;
         a.N = plan->Nq + plan->Nfab;
@@ -694,8 +698,9 @@ int kda_proj_run(const kda_plan *plan, const void *x, const void *W_packed, cons
         fb.row0 = plan->Nq;
         kp_cfg c = cq;
         c.flags &= ~KP_FLAG_FUSE_FB;
-        if ((e = tc05_launch(a, c, plan->sms, ms, &fb, &so)) != cudaSuccess)
-            return cuda_fail(e, "single-launch projection");
+        e = c.kind == KP_KIND_CC ? cc_proj_launch(a, c, so, fb, ms)
+                                 : tc05_launch(a, c, plan->sms, ms, &fb, &so);
+        if (e != cudaSuccess) return cuda_fail(e, "single-launch projection");
         return KP_OK;
     }
 

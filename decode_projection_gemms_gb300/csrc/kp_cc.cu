@@ -50,10 +50,10 @@ cudaError_t ensure_smem_attr(const void *fn) {
 bool cc_supported(int M, int K, const kp_cfg &c) {
     if (M < 1 || M > 16 || K < 8 || (K & 7)) return false;
     if (c.split_k < 1 || c.split_k > K / 8) return false;
-    if (c.block < 32 || c.block > 256 || (c.block & 31)) return false;
+    if (c.block < 32 || c.block > 512 || (c.block & 31)) return false;
     if (!cc_kernel(M, c.rows, c.k_unroll, KP_BF16)) return false;  // same set for fp16
     const int ks = cc_slice(K, c.split_k);
-    return static_cast<long long>(M) * ks * 4 <= kMaxSmem;  // x slice fits in shared memory
+    return static_cast<long long>(M) * ks * 2 <= kMaxSmem;  // x slice (16-bit) fits in shared memory
 }
 
 Scratch cc_scratch(int M, int N, int K, const kp_cfg &c) {
@@ -68,6 +68,63 @@ Scratch cc_scratch(int M, int N, int K, const kp_cfg &c) {
     return s;
 }
 
+bool cc_proj_supported(int M, int K, int N, const kp_cfg &c, int n_split) {
+    if (M < 1 || M > 8 || c.kind != KP_KIND_CC || c.split_k != 1 || !cc_supported(M, K, c)) return false;
+    if (!cc_table_proj[M - 1][cc_variant(c.rows, c.k_unroll)]) return false;
+    const int rows_cta = (c.block / 32) * c.rows;
+    if (rows_cta > kFaWidth || kFaWidth % rows_cta) return false;   // F_A rows = whole CTAs
+    if (kFaWidth / rows_cta > 8) return false;                        // portable cluster size
+    return n_split > 0 && n_split % kFaWidth == 0 && N - n_split >= kFaWidth;
+}
+
+cudaError_t cc_proj_launch(const GemmArgs &a, const kp_cfg &c, const SplitOut &so, const FusedFB &fb,
+                           cudaStream_t stream) {
+    if (!cc_proj_supported(a.M, a.K, a.N, c, so.n_split) || fb.row0 != so.n_split ||
+        a.dtype != KP_BF16 || a.res)
+        return cudaErrorInvalidValue;
+    CCKernelFn fn = cc_table_proj[a.M - 1][cc_variant(c.rows, c.k_unroll)];
+    CCParams p;
+    p.a = a;
+    p.Ks = cc_slice(a.K, 1);
+    p.S = 1;
+    p.rows_cta = (c.block / 32) * c.rows;
+    CCProj &q = p.proj;
+    q.n_split = so.n_split;
+    q.y2 = so.y2;
+    q.ldy2 = so.ldy2;
+    q.fa_ctas = kFaWidth / p.rows_cta;
+    q.fa_tile0 = so.n_split / p.rows_cta;
+    const int tiles = (a.N + p.rows_cta - 1) / p.rows_cta;
+    q.n_tiles = (tiles + q.fa_ctas - 1) / q.fa_ctas * q.fa_ctas;
+    q.Wfb = fb.W;
+    q.N_fb = fb.N;
+    q.yfb = fb.y;
+    q.ldfb = fb.ld;
+    const size_t smem = static_cast<size_t>(a.M) * p.Ks * 2;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(q.n_tiles, 1, 1);
+    cfg.blockDim = dim3(c.block, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = q.fa_ctas;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    if (c.flags & KP_FLAG_PDL) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, fn, p);
+}
+
 cudaError_t cc_launch(const GemmArgs &a, const kp_cfg &c, cudaStream_t stream) {
     if (!cc_supported(a.M, a.K, c)) return cudaErrorInvalidValue;
     CCKernelFn fn = cc_kernel(a.M, c.rows, c.k_unroll, a.dtype);
@@ -78,7 +135,7 @@ cudaError_t cc_launch(const GemmArgs &a, const kp_cfg &c, cudaStream_t stream) {
     p.S = (a.K + p.Ks - 1) / p.Ks;
     p.rows_cta = (c.block / 32) * c.rows;
     const int tiles = (a.N + p.rows_cta - 1) / p.rows_cta;
-    const size_t smem = static_cast<size_t>(a.M) * p.Ks * sizeof(float);
+    const size_t smem = static_cast<size_t>(a.M) * p.Ks * 2;   // x slice, 16-bit elements
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn));
     if (e != cudaSuccess) return e;
 

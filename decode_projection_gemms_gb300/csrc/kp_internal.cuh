@@ -62,6 +62,13 @@ struct SplitOut {
     int64_t ldy2;
 };
 
+// CUDA-core single-launch projection (kp_cc.cu): one K slice over the packed
+// weight, rows >= split.n_split to split.y2, F_B computed by the cluster of
+// the F_A rows (fb.row0 == split.n_split); bf16, M <= 8.
+bool cc_proj_supported(int M, int K, int N, const kp_cfg &c, int n_split);
+cudaError_t cc_proj_launch(const GemmArgs &a, const kp_cfg &c, const SplitOut &split, const FusedFB &fb,
+                           cudaStream_t s);
+
 // tcgen05 cluster split-K kernel (kp_tc05.cu)
 bool tc05_supported(int M, int N, int K, const kp_cfg &c);
 bool tc05_fusable(int M, const kp_cfg &c);
@@ -129,6 +136,28 @@ __device__ __forceinline__ float elem_widen(uint16_t b, int dtype) {
 }
 __device__ __forceinline__ uint16_t elem_round(float f, int dtype) {
     return dtype == KP_FP16 ? elem_round<KP_FP16>(f) : elem_round<KP_BF16>(f);
+}
+
+// acc + w.lo * x.lo, then + w.hi * x.hi, for two 16-bit elements (bf16 or fp16,
+// T) packed in each 32-bit word. The mixed-precision FMA takes the 16-bit
+// operands directly: their product is exact in fp32 (8- or 11-bit
+// significands) and each step rounds once, exactly as widening both to fp32
+// and calling fmaf would.
+template <int T>
+__device__ __forceinline__ float fma_pair(uint32_t w, uint32_t x, float acc) {
+    if constexpr (T == KP_FP16)
+        asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+            "mov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+            "fma.rn.f32.f16 %0, wl, xl, %0;\n\tfma.rn.f32.f16 %0, wh, xh, %0;\n\t}"
+            : "+f"(acc)
+            : "r"(w), "r"(x));
+    else
+        asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
+            "mov.b32 {wl, wh}, %1;\n\tmov.b32 {xl, xh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, wl, xl, %0;\n\tfma.rn.f32.bf16 %0, wh, xh, %0;\n\t}"
+            : "+f"(acc)
+            : "r"(w), "r"(x));
+    return acc;
 }
 
 // Programmatic dependent launch. Without the launch attribute both are no-ops.
@@ -217,6 +246,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // ---- TMA --------------------------------------------------------------------
+// Contiguous bulk copy global -> this CTA's shared memory, completing `bytes`
+// of transaction on the mbarrier. Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const void *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -125,7 +125,7 @@ typedef struct kp_cfg {
                          128-feature tile, each streaming 1/split_k of K
                          (1, 2, 4, 8, 16; reduced in distributed shared
                          memory, no scratch) */
-    int32_t block;    /* CC, SMALLK: threads per CTA (multiple of 32; CC <= 256,
+    int32_t block;    /* CC, SMALLK: threads per CTA (multiple of 32; CC <= 512,
                          SMALLK <= 256) */
     int32_t rows;     /* CC: output rows per warp (1, 2, 4, 8);
                          SMALLK: output rows per CTA (1..64);
@@ -207,8 +207,8 @@ KP_API int kp_table_size(void);
  * skinny_gemm); the call calls no cudaMalloc, cudaFree or allocating library
  * routine.
  *   - Limits: M <= 16 (CUDA-core kernel). The kernel stages x's K slice in
- *     shared memory (M * ceil(K / split_k) * 4 bytes, at most 200 KiB), so a
- *     shape needs split_k >= ceil(M * K * 4 / 204800); its split-K partial
+ *     shared memory (M * ceil(K / split_k) * 2 bytes, at most 200 KiB), so a
+ *     shape needs split_k >= ceil(M * K * 2 / 204800); its split-K partial
  *     sums (split_k * M * N floats when split_k > 1) must fit in
  *     KP_NOALLOC_SCRATCH_FLOATS and its row tiles (ceil(N / 32) with the
  *     default configuration) in KP_NOALLOC_TICKETS. With cfg NULL (or kind
@@ -216,7 +216,7 @@ KP_API int kp_table_size(void);
  *     it until the partial sums fit, then raises it again if x's slice does
  *     not fit in shared memory; a shape whose smallest such split_k needs
  *     more partial sums than the array holds (e.g. M = 16, K = 16384,
- *     N = 8192: split_k >= 6, 786432 floats) returns KP_ETOOBIG. An explicit
+ *     N = 16384: split_k >= 3, 786432 floats) returns KP_ETOOBIG. An explicit
  *     cfg must be kind KP_KIND_CC.
  *   - Ordering: with cfg NULL the kernel launches without programmatic
  *     dependent launch, so x and W may both come from the kernel just before

@@ -80,7 +80,7 @@ def test_cc_shapes(M, N, K):
 
 def test_cc_block_sizes_and_unsplit():
     x, W = gemm_case(3, 777, 2048, seed=5)
-    for block in (32, 128, 256):
+    for block in (32, 128, 256, 512):
         for S in (1, 2, 16):
             check_gemm(x, W, KpCfg.make("cc", split_k=S, block=block, rows=2, k_unroll=2), "cc")
 
@@ -477,11 +477,79 @@ def test_kda_single_launch(plan, M, C, nkb):
         plan.set_overlap(-1)
 
 
+CC_SINGLE = [KpCfg.make("cc", split_k=1, block=256, rows=2, k_unroll=4),   # 16 rows: cluster of 8
+             KpCfg.make("cc", split_k=1, block=512, rows=1, k_unroll=4),   # 16 rows
+             KpCfg.make("cc", split_k=1, block=256, rows=4, k_unroll=2),   # 32 rows: cluster of 4
+             KpCfg.make("cc", split_k=1, block=128, rows=4, k_unroll=1)]   # 16 rows, 4 warps
+
+
+def _single_launch_cc_check(p, M, cfg, K, Nq, Nfab, Nfb, layer, seed):
+    x, wp, wfb = kda_inputs(M, layer=layer, seed=seed, K=K, Nq=Nq, Nfab=Nfab, Nfb=Nfb)
+    xd, wpd, wfbd = x.cuda(), wp.cuda(), wfb.cuda()
+    aux = torch.cuda.Stream()
+    evs = binding.make_events()
+    p.set_config(binding.BRANCH_QKVG, M, cfg)
+    assert p.overlap_at(M) in (0, 1, 2)
+    outs = (poisoned((M, Nq)), poisoned((M, Nfab)), poisoned((M, Nfb)))
+    p.set_overlap(2)
+    p.run(xd, wpd, wfbd, *outs, aux_stream=aux, events=evs)
+    torch.cuda.synchronize()
+    check_kda(outs, x, wp, wfb, Nq, Nfab, f"CUDA-core single launch {cfg.as_dict()} M={M}")
+    # each part equals the same CUDA-core kernel run on its own rows, and F_B
+    # the small-K kernel (same k order) on the GPU's F_A
+    q = binding.skinny_gemm(xd, wpd[:Nq].contiguous(), cfg=cfg)
+    f = binding.skinny_gemm(xd, wpd[Nq:].contiguous(), cfg=cfg)
+    b = binding.skinny_gemm(outs[1][:, :128].contiguous(), wfbd,
+                            cfg=KpCfg.make("smallk", block=256, rows=16))
+    torch.cuda.synchronize()
+    assert torch.equal(q, outs[0]) and torch.equal(f, outs[1]) and torch.equal(b, outs[2])
+    # captured and replayed
+    again = (poisoned((M, Nq)), poisoned((M, Nfab)), poisoned((M, Nfb)))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        p.run(xd, wpd, wfbd, *again, aux_stream=aux, events=evs)
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for a_, b_ in zip(outs, again):
+        assert torch.equal(a_, b_)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("ci", range(len(CC_SINGLE)))
+def test_kda_single_launch_cuda_core(plan, M, ci):
+    """Mode 2 with a one-slice CUDA-core Q/K/V/G configuration: one launch over
+    the packed weight; the CTAs of the F_A rows form a cluster that computes
+    F_B from the bf16 F_A it exchanges in distributed shared memory."""
+    saved = [plan.get_config(b, M) for b in range(3)]
+    try:
+        _single_launch_cc_check(plan, M, CC_SINGLE[ci], 7168, 4096, 136, 1024, layer=9, seed=10)
+    finally:
+        for b, c in enumerate(saved):
+            plan.set_config(b, M, c)
+        plan.set_overlap(-1)
+
+
+def test_kda_single_launch_cuda_core_ragged():
+    """Ragged packed shape: the last tile of the F_A/beta rows is partly past
+    N, whole padding CTAs leave at once, K = 1032 is not a multiple of the
+    loop's step, and N_fb = 200 does not divide evenly over the cluster."""
+    p = binding.KdaPlan(K=1032, N_qkvg=256, N_fab=136, N_fb=200, max_M=8)
+    try:
+        for M, cfg in ((1, CC_SINGLE[0]), (5, CC_SINGLE[1]), (8, CC_SINGLE[2]), (3, CC_SINGLE[3])):
+            _single_launch_cc_check(p, M, cfg, 1032, 256, 136, 200, layer=2, seed=11)
+    finally:
+        p.close()
+
+
 def test_single_launch_falls_back_for_a_cuda_core_config(plan):
+    # 6 rows per CTA (3 warps x 2) do not tile the 128 F_A rows: no single-launch
+    # form, so mode 2 runs the overlapped path
     M = 2
     saved = plan.get_config(binding.BRANCH_QKVG, M)
     try:
-        plan.set_config(binding.BRANCH_QKVG, M, KpCfg.make("cc", split_k=1, rows=2, k_unroll=4))
+        plan.set_config(binding.BRANCH_QKVG, M, KpCfg.make("cc", split_k=1, block=96, rows=2,
+                                                           k_unroll=4))
         x, wp, wfb = kda_inputs(M, layer=7, seed=9)
         outs = _run_mode(plan, x.cuda(), wp.cuda(), wfb.cuda(), 2, torch.cuda.Stream(),
                          binding.make_events())

@@ -77,11 +77,12 @@ def test_noalloc_rejects_what_does_not_fit(lib):
     too_many_slices = KpCfg.make("cc", split_k=28, block=256, rows=4, k_unroll=1)
     assert _noalloc(lib, x, W, y, too_many_slices) == binding.KP_ETOOBIG
     assert b"fixed scratch" in lib.kp_last_error()
-    # the entry point's own choice cannot fit either: x's slice needs
-    # split_k >= 6 at K = 16384, and 6 * 16 * 8192 partial sums exceed the array
+    # the entry point's own choice cannot fit either: x's slice (16 x 16384
+    # 16-bit elements) needs split_k >= 3 to fit in 200 KiB of shared memory,
+    # and 3 * 16 * 16384 partial sums exceed the array
     xk = gen_x(16, 16384, seed=4).cuda()
-    Wk = torch.zeros((8192, 16384), dtype=torch.bfloat16, device="cuda")
-    yk = torch.empty((16, 8192), dtype=torch.bfloat16, device="cuda")
+    Wk = torch.zeros((16384, 16384), dtype=torch.bfloat16, device="cuda")
+    yk = torch.empty((16, 16384), dtype=torch.bfloat16, device="cuda")
     assert _noalloc(lib, xk, Wk, yk, None) == binding.KP_ETOOBIG
     del Wk
     x17 = gen_x(17, 7168, seed=3).cuda()
