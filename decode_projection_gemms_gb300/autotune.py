@@ -144,13 +144,13 @@ def sweep_candidates(M: int, N: int, K: int, sms: int):
     if K <= 256:
         out += [KpCfg.make("smallk", block=256, rows=r) for r in (8, 16)]
     if M <= 16:
-        for (R, U) in ((1, 4), (2, 4), (4, 2)):
+        for (R, U, block) in ((1, 4, 256), (2, 4, 256), (4, 2, 256), (1, 4, 512), (2, 4, 512)):
             if R * M > 64:
                 continue
-            tiles = math.ceil(N / (8 * R))
-            for waves in (2, 4):
+            tiles = math.ceil(N / (block // 32 * R))
+            for waves in (1, 2, 4):
                 S = max(1, min(max(1, K // 256), round(waves * sms / tiles)))
-                out.append(KpCfg.make("cc", split_k=S, block=256, rows=R, k_unroll=U))
+                out.append(KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U))
     KB = math.ceil(K / 64)
     for rows in (128, 256) if M >= 32 else (128,):
         T = math.ceil(N / rows)

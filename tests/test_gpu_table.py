@@ -1,0 +1,158 @@
+"""The shipped autotune table against fresh measurements on this GPU.
+
+The table (tune/gb300_table.txt) was written by the autotuner on a GB300; these
+tests re-time some of its choices beside their alternatives and require the
+table's choice to be within measurement noise of the fastest. That is the
+check "[Kimi-K3] Overlap low-M TP8 KDA projections" describes for its
+configuration table (section 实现拆解, item 5: the chosen configurations match
+a measured table).
+
+Timing: CUDA graphs of back-to-back calls over a weight stack larger than the
+L2 cache (one layer per call, so weights come from HBM as in decode),
+replayed between CUDA events on the capturing stream; the median of three
+runs. A choice passes when it is no more than 8 % slower than the fastest
+alternative (box-to-box and run-to-run spread of these timings is a few
+percent).
+"""
+import math
+import statistics
+
+import pytest
+import torch
+
+from decode_projection_gemms_gb300 import binding
+from decode_projection_gemms_gb300.binding import KpCfg
+
+pytestmark = pytest.mark.gpu
+
+L2_BYTES = 129 * 1024 * 1024
+NOISE = 1.08
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from decode_projection_gemms_gb300.build import build
+    build()
+    binding.load()
+    binding.table_load()
+    yield
+    assert binding.device_error() == 0
+
+
+def _graph_time(body, n_calls, stream, reps=10):
+    with torch.cuda.stream(stream):
+        body(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_calls):
+            body(i)
+    res = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            b.synchronize()
+            res.append(a.elapsed_time(b) * 1e3 / (reps * n_calls))
+    return statistics.median(res)
+
+
+@pytest.fixture(scope="module")
+def kda_stack():
+    K, Nq, Nfab, Nfb = 7168, 4096, 136, 1024
+    layers = 48
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    wp = (torch.randn((layers, Nq + Nfab, K), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    wfb = (torch.randn((layers, Nfb, 128), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    plan = binding.KdaPlan(K, Nq, Nfab, Nfb, max_M=128)
+    yield plan, wp, wfb
+    plan.close()
+    del wp, wfb
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 64, 128])
+def test_projection_mode_matches_measurement(kda_stack, M):
+    """The table's mode at M (sequential, overlapped or single launch) is the
+    fastest of the three, within noise, with the table's configurations."""
+    plan, wp, wfb = kda_stack
+    x = torch.randn((M, 7168), device="cuda").to(torch.bfloat16)
+    outs = plan.outputs(M)
+    main, aux = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(main):
+        evs = binding.make_events()
+    chosen = plan.overlap_at(M)
+    times = {}
+    try:
+        for mode in (0, 1, 2):
+            plan.set_overlap(mode)
+            times[mode] = _graph_time(
+                lambda i: plan.run(x, wp[i], wfb[i], *outs, aux_stream=aux, events=evs),
+                wp.shape[0], main)
+    finally:
+        plan.set_overlap(-1)
+    assert times[chosen] <= NOISE * min(times.values()), f"M={M}: table mode {chosen}, times {times}"
+
+
+def _alternatives(M, N, K, pick):
+    """A few configurations around the table's pick: the other kernel kinds'
+    usual settings and the pick with its split factor and stage depth moved."""
+    out = []
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T = math.ceil(N / 128)
+    for C in (1, 2, 4, 8, 16):
+        if T * C <= 2 * sms and C <= math.ceil(K / 64):
+            out.append(KpCfg.make("tc05", split_k=C, k_unroll=2, producers=2))
+    if M <= 16:
+        for (R, U, block) in ((2, 4, 256), (1, 4, 512), (4, 2, 256)):
+            tiles = math.ceil(N / (block // 32 * R))
+            S = max(1, min(max(1, K // 256), round(sms / tiles)))
+            out.append(KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U))
+    if K <= 256:
+        out.append(KpCfg.make("smallk", block=256, rows=16))
+    if pick.kind == binding.KIND_TC05:
+        for st in (2, 3):
+            c = KpCfg.from_buffer_copy(pick)
+            c.stages = st
+            out.append(c)
+    valid = []
+    for c in out:
+        try:
+            binding.scratch_bytes(M, N, K, c, sms)
+            valid.append(c)
+        except binding.KdaProjError:
+            pass
+    return valid
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1024, 7168), (4, 8192, 1024), (16, 136, 16384),
+                                   (64, 512, 7168), (2, 4096, 16384)])
+def test_gemm_entry_matches_measurement(M, N, K):
+    """A plain skinny GEMM entry of the shape sweep: the table's configuration
+    is within noise of the fastest of the alternatives around it."""
+    pick = binding.select_config(M, N, K)
+    layers = max(4, math.ceil(4 * L2_BYTES / (N * K * 2)))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    W = (torch.randn((layers, N, K), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    x = torch.randn((M, K), device="cuda").to(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    try:
+        t_pick = _graph_time(lambda i: binding.skinny_gemm(x, W[i], y, cfg=pick), layers, s)
+        others = {}
+        for c in _alternatives(M, N, K, pick):
+            others[str(c.as_dict())] = _graph_time(lambda i: binding.skinny_gemm(x, W[i], y, cfg=c),
+                                                   layers, s)
+    finally:
+        del W
+        torch.cuda.empty_cache()
+    best = min(others.values()) if others else t_pick
+    assert t_pick <= NOISE * best, f"M={M} N={N} K={K}: pick {pick.as_dict()} {t_pick:.3f} us, " \
+                                   f"alternatives {others}"
