@@ -658,8 +658,9 @@ def run_handoff(args, plan, wp_stack, wfb_stack, xs, outs, dev, main, aux, evs, 
 def run_eager(args, plan, wp_stack, wfb_stack, xs, outs, main, aux, evs, dist, m_e=(1, 16, 128)):
     """The projection called eagerly (no graph): host time per call to enqueue
     it, through the Python binding and through the bare C ABI (ctypes with
-    prepared arguments), and the device time per call of the eager chain of
-    48 calls (one layer each)."""
+    prepared arguments), and the device time per call of each eager chain of
+    48 calls (one layer each); a chain whose host time per call exceeds the
+    kernels' is paced by the host."""
     import ctypes
     import torch
     from decode_projection_gemms_gb300 import binding
@@ -678,7 +679,7 @@ def run_eager(args, plan, wp_stack, wfb_stack, xs, outs, main, aux, evs, dist, m
                 ctypes.c_void_p(wfb_stack[layer].data_ptr()), ctypes.c_void_p(oq.data_ptr()),
                 ctypes.c_void_p(of.data_ptr()), ctypes.c_void_p(ob.data_ptr()), M, ms, ax, ev)
                for layer in range(L)]
-        host_py, host_c, dev_us = [], [], []
+        host_py, host_c, dev_py, dev_c = [], [], [], []
         with torch.cuda.stream(main):
             for rep in range(6):
                 torch.cuda.synchronize()
@@ -699,12 +700,13 @@ def run_eager(args, plan, wp_stack, wfb_stack, xs, outs, main, aux, evs, dist, m
                 torch.cuda.synchronize()
                 if rep >= 2:   # the first pair warms up
                     (host_py if rep % 2 == 0 else host_c).append((t1 - t0) * 1e6 / L)
-                    dev_us.append(a.elapsed_time(b) * 1e3 / L)
+                    (dev_py if rep % 2 == 0 else dev_c).append(a.elapsed_time(b) * 1e3 / L)
         vals = reduce_max([statistics.median(host_py), statistics.median(host_c),
-                           statistics.median(dev_us)], dist)
+                           statistics.median(dev_py), statistics.median(dev_c)], dist)
         out["per_m"][str(M)] = {"host_us_per_call_binding": round(vals[0], 2),
                                 "host_us_per_call_c_abi": round(vals[1], 2),
-                                "device_us_per_call_eager": round(vals[2], 3)}
+                                "device_us_per_call_eager_binding": round(vals[2], 3),
+                                "device_us_per_call_eager_c_abi": round(vals[3], 3)}
     return out
 
 

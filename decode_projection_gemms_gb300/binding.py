@@ -127,6 +127,10 @@ def last_error() -> str:
 
 
 def _bf16_2d(t: torch.Tensor, name: str):
+    # the common case in a few cheap checks; the rest only to name the problem
+    if type(t) is torch.Tensor and t.dtype is torch.bfloat16 and t.is_cuda and t.dim() == 2 \
+            and t.is_contiguous():
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != torch.bfloat16:
@@ -292,6 +296,8 @@ class KdaPlan:
                  max_M: int = 256):
         self.K, self.N_qkvg, self.N_fab, self.N_fb, self.max_M = K, N_qkvg, N_fab, N_fb, max_M
         self._lib = load()
+        self._run = self._lib.kda_proj_run
+        self._ev_key, self._ev_arr = None, None
         h = ctypes.c_void_p()
         _check(self._lib.kda_proj_plan(K, N_qkvg, N_fab, N_fb, max_M, ctypes.byref(h)))
         self._h = h
@@ -334,12 +340,12 @@ class KdaPlan:
         _bf16_2d(x, "x")
         _bf16_2d(W_packed, "W_packed")
         _bf16_2d(W_fb, "W_fb")
-        M = x.shape[0]
-        if x.shape[1] != self.K:
+        M, kx = x.shape
+        if kx != self.K:
             raise ValueError(f"x must be [M, {self.K}]")
-        if tuple(W_packed.shape) != (self.N_qkvg + self.N_fab, self.K):
+        if W_packed.shape != (self.N_qkvg + self.N_fab, self.K):
             raise ValueError(f"W_packed must be {(self.N_qkvg + self.N_fab, self.K)}")
-        if tuple(W_fb.shape) != (self.N_fb, 128):
+        if W_fb.shape != (self.N_fb, 128):
             raise ValueError(f"W_fb must be {(self.N_fb, 128)}")
         if out_qkvg is None or out_fab is None or out_fb is None:
             oq, of, ob = self.outputs(M, x.device)
@@ -349,16 +355,22 @@ class KdaPlan:
         for t, n, shape in ((out_qkvg, "out_qkvg", (M, self.N_qkvg)), (out_fab, "out_fab", (M, self.N_fab)),
                             (out_fb, "out_fb", (M, self.N_fb))):
             _bf16_2d(t, n)
-            if tuple(t.shape) != shape:
+            if t.shape != shape:
                 raise ValueError(f"{n} must be {shape}")
         ev = None
         aux = None
         if aux_stream is not None and events is not None:
-            aux = ctypes.c_void_p(int(aux_stream.cuda_stream))
-            ev = (ctypes.c_void_p * 2)(int(events[0].cuda_event), int(events[1].cuda_event))
-        _check(self._lib.kda_proj_run(self._h, x.data_ptr(), W_packed.data_ptr(), W_fb.data_ptr(),
-                                      out_qkvg.data_ptr(), out_fab.data_ptr(), out_fb.data_ptr(), M,
-                                      _stream_handle(stream), aux, ev))
+            aux = aux_stream.cuda_stream
+            key = (events[0].cuda_event, events[1].cuda_event)
+            if self._ev_key != key:   # the handle array, reused while the events are
+                self._ev_key = key
+                self._ev_arr = (ctypes.c_void_p * 2)(*key)
+            ev = self._ev_arr
+        rc = self._run(self._h, x.data_ptr(), W_packed.data_ptr(), W_fb.data_ptr(),
+                       out_qkvg.data_ptr(), out_fab.data_ptr(), out_fb.data_ptr(), M,
+                       _stream_handle(stream), aux, ev)
+        if rc:
+            _check(rc)
         if check:
             check_device(stream)
         return out_qkvg, out_fab, out_fb
