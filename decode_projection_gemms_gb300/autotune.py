@@ -45,6 +45,19 @@ def cc_candidates(M: int, N: int, K: int, sms: int):
             for waves in (1, 2, 4, 8):
                 S = max(1, min(K // 256 if K >= 256 else 1, round(waves * sms / tiles)))
                 out.append(KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U))
+    # Tiles sized for whole waves: for one or two CTAs per SM and S K slices,
+    # the rows per CTA (whole warps of R rows) that bring tiles x S closest to
+    # SMs x CTAs-per-SM without a partial wave.
+    for (R, U) in ((1, 4), (2, 4), (2, 2), (4, 1), (4, 2)):
+        for occ in (1, 2):
+            for S in (1, 2, 3, 4):
+                if S > max(1, K // 256):
+                    continue
+                target = max(1, sms * occ // S)
+                warps = math.ceil(math.ceil(N / target) / R)
+                block = 32 * warps
+                if 32 <= block <= 512 // occ:
+                    out.append(KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U))
     # dedupe
     seen, uniq = set(), []
     for c in out:

@@ -174,21 +174,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     // The fused F_B tile (if any) is dispatched first: its cluster has the
     // longest epilogue.
-    int tile = (static_cast<int>(blockIdx.x) / C + p.tile_rot) % p.n_tiles;
-    // Token tile of this CTA: tokens [m0, m0 + Mloc). Blocks are dispatched
-    // in linear order (x fastest); without clusters the linear id is remapped
-    // so that the token tiles of one feature tile are consecutive: they run in
-    // the same wave and all but the first read the tile's weights from L2
-    // (with feature tiles fastest, a grid larger than one wave re-streamed
-    // every weight tile from HBM in the next wave).
-    int ttile = static_cast<int>(blockIdx.y);
-    if (kTiled && C == 1) {
-        const int id = static_cast<int>(blockIdx.x + blockIdx.y * gridDim.x);
-        ttile = id % static_cast<int>(gridDim.y);
-        tile = id / static_cast<int>(gridDim.y);
-    }
+    const int tile = (static_cast<int>(blockIdx.x) / C + p.tile_rot) % p.n_tiles;
     const bool fused = (p.fb_tile >= 0 && tile == p.fb_tile);
-    const int m0 = kTiled ? ttile * p.Mpad : 0;
+    // Token tile of this CTA: tokens [m0, m0 + Mloc), along the grid's y axis.
+    const int m0 = kTiled ? static_cast<int>(blockIdx.y) * p.Mpad : 0;
     const int Mloc = kTiled ? min(p.M - m0, p.Mpad) : p.M;
     const int kb0 = static_cast<int>((static_cast<long long>(p.KB) * rank) / C);
     const int kb1 = static_cast<int>((static_cast<long long>(p.KB) * (rank + 1)) / C);
