@@ -148,7 +148,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // grid's y axis.
 // kWide = false: a CTA owns 128 feature rows; true: 256, as two 128-row MMAs
 // on the same x operand into two TMEM accumulators (x per weight byte halves).
-template <bool kGeneral, bool kTiled, bool kWide>
+// kFB: the launch fuses F_B into one cluster (bf16, one token tile); the other
+// instantiations carry none of that code.
+template <bool kGeneral, bool kTiled, bool kWide, bool kFB = false>
 __global__ void __launch_bounds__(kThreads, 1)
     tc05_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
                 const __grid_constant__ CUtensorMap tmx3, const __grid_constant__ CUtensorMap tmfb,
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The fused F_B tile (if any) is dispatched first: its cluster has the
     // longest epilogue.
     const int tile = (static_cast<int>(blockIdx.x) / C + p.tile_rot) % p.n_tiles;
-    const bool fused = (p.fb_tile >= 0 && tile == p.fb_tile);
+    const bool fused = kFB && p.fb_tile >= 0 && tile == p.fb_tile;
     // Token tile of this CTA: tokens [m0, m0 + Mloc), along the grid's y axis.
     const int m0 = kTiled ? static_cast<int>(blockIdx.y) * p.Mpad : 0;
     const int Mloc = kTiled ? min(p.M - m0, p.Mpad) : p.M;
@@ -184,7 +186,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_st = (kb1 - kb0 + p.nkb - 1) / p.nkb;  // stages of work for this CTA
     // fused F_B tiles of this CTA: rank, rank + C, ...
     const int my_fb = fused && rank < p.fb_tiles ? (p.fb_tiles - rank + C - 1) / C : 0;
-
+    // With one F_B tile, its W_fb (two 16 KB boxes) goes into the stage buffer
+    // whose last main-loop use ends first (stage n_st - S; a buffer the main
+    // loop never uses if n_st < S), provided that buffer lies past the region
+    // the epilogue writes (partial tile, F_A operand). Its load then starts
+    // while the last stages are still in the tensor cores, instead of after
+    // the whole main loop: the fused cluster's epilogue is the launch's
+    // longest, and its tail no longer waits for these loads.
+    int fb_early = -1;
+    if (my_fb == 1 && p.stage_bytes >= 2 * kWBlockBytes) {
+        const int b = n_st < S ? n_st : (n_st - S) % S;
+        if (b < S && static_cast<uint32_t>(b) * p.stage_bytes >= p.off_wfb) fb_early = b;
+    }
     // producer index of this warp's lane 0 (-1: not a producer)
     const int pidx = (warp == 0) ? 0 : (warp >= 2 && warp - 1 < p.producers) ? warp - 1 : -1;
     const int P = p.producers;
@@ -291,7 +304,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = first; s < n_st; ++s)
                 drain_wait(smem_u32(full + (s % S)), static_cast<uint32_t>((s / S) & 1));
         }
-        if (pidx == 0 && my_fb > 0) {
+        if (pidx == 0 && fb_early >= 0) {
+            // the early W_fb buffer: free once stage n_st - S's MMAs are done
+            if (n_st >= S)
+                mbar_wait_bounded(smem_u32(empty + fb_early), static_cast<uint32_t>(((n_st - S) / S) & 1),
+                                  abort_flag, p.err, DEV_TIMEOUT_EMPTY);
+            const uint32_t dst = base + static_cast<uint32_t>(fb_early) * p.stage_bytes;
+            mbar_expect_tx(smem_u32(fbw), 2 * kWBlockBytes);
+            for (int j = 0; j < 2; ++j)
+                tma_load_2d(dst + j * kWBlockBytes, &tmfb, smem_u32(fbw), j * kBlockK, rank * kTileN,
+                            policy_evict_last());
+        } else if (pidx == 0 && my_fb > 0) {
             // The pipeline memory is free once every main-loop MMA has
             // completed: fetch this CTA's W_fb tiles (as many as have a
             // buffer) while the epilogue and the cluster reduction run.
@@ -526,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int A = p.fb_accs;
         const uint32_t b_base = base + p.off_bfa;
         auto a_base = [&](int i) {
+            if (fb_early >= 0) return base + static_cast<uint32_t>(fb_early) * p.stage_bytes;   // i == 0
             return base + p.off_wfb + static_cast<uint32_t>(i % B) * 2 * kWBlockBytes;
         };
         if (warp == 0 && lane == 0) {
@@ -948,7 +972,8 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
             for (auto fn : {tc05_kernel<false, false, false>, tc05_kernel<true, false, false>,
                             tc05_kernel<false, true, false>, tc05_kernel<true, true, false>,
                             tc05_kernel<false, false, true>, tc05_kernel<true, false, true>,
-                            tc05_kernel<false, true, true>, tc05_kernel<true, true, true>}) {
+                            tc05_kernel<false, true, true>, tc05_kernel<true, true, true>,
+                            tc05_kernel<false, false, false, true>, tc05_kernel<false, false, true, true>}) {
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
                 if (e == cudaSuccess)
@@ -1003,7 +1028,9 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
          {tc05_kernel<false, true, false>, tc05_kernel<false, true, true>}},
         {{tc05_kernel<true, false, false>, tc05_kernel<true, false, true>},
          {tc05_kernel<true, true, false>, tc05_kernel<true, true, true>}}};
-    const Fn fn = kernels[general][tiled][rt == 2 * kTileN];
+    // the fused F_B has its own instantiations (bf16, one token tile: checked above)
+    const Fn fn = fb ? (rt == 2 * kTileN ? tc05_kernel<false, false, true, true> : tc05_kernel<false, false, false, true>)
+                     : kernels[general][tiled][rt == 2 * kTileN];
     return cudaLaunchKernelEx(&cfg, fn, mw, mx, mx3, mfb, p);
 }
 
