@@ -179,7 +179,7 @@ static kp_cfg select_config(int M, int N, int K, int sms, int *overlap) {
 static Scratch scratch_of(int M, int N, int K, const kp_cfg &c, int sms) {
     switch (c.kind) {
     case KP_KIND_CC: return cc_scratch(M, N, K, c);
-    case KP_KIND_TC05: return tc05_scratch(M < 256 ? M : 256, N, K, c, sms);
+    case KP_KIND_TC05: return tc05_scratch(M, N, K, c, sms);
     default: return Scratch();
     }
 }
@@ -267,6 +267,14 @@ static BranchShape branch_shape(const kda_plan *p, int b) {
     if (b == KP_BRANCH_QKVG) return {p->Nq, p->K};
     if (b == KP_BRANCH_FAB) return {p->Nfab, p->K};
     return {p->Nfb, 128};
+}
+
+// Scratch a branch's configuration needs at M; the Q/K/V/G branch's also
+// serves the single launch over the packed weight (N_qkvg + N_fab rows).
+static Scratch branch_scratch(const kda_plan *p, int b, int M, const kp_cfg &c) {
+    const BranchShape sh = branch_shape(p, b);
+    const int N = b == KP_BRANCH_QKVG ? p->Nq + p->Nfab : sh.N;
+    return scratch_of(M, N, sh.K, c, p->sms);
 }
 
 static void free_plan_memory(kda_plan *p) {
@@ -552,9 +560,22 @@ int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_plan **
             }
             p->cfg[b][M] = c;
             if (b == KP_BRANCH_QKVG) p->overlap[M] = static_cast<uint8_t>(ov < 0 ? 0 : ov > 2 ? 1 : ov);
-            Scratch s = scratch_of(M, sh.N, sh.K, c, p->sms);
+            Scratch s = branch_scratch(p, b, M, c);
             if (s.floats > need[b].floats) need[b].floats = s.floats;
             if (s.counters > need[b].counters) need[b].counters = s.counters;
+        }
+        // Room for any tcgen05 configuration at up to 256 tokens (clusters of
+        // up to 16, 128 or 256 rows per CTA), so kda_proj_set_config can swap
+        // them in: the split-K partial tiles are C * Mpad * rows fp32 per tile.
+        const int Mh = max_M < 256 ? max_M : 256;
+        for (int rows : {128, 256}) {
+            if (b == KP_BRANCH_FB) break;   // K = 128: two K blocks, no wide split
+            kp_cfg c = {};
+            c.kind = KP_KIND_TC05;
+            c.split_k = 16;
+            c.rows = rows;
+            Scratch s = branch_scratch(p, b, Mh, c);
+            if (s.floats > need[b].floats) need[b].floats = s.floats;
         }
     }
     cudaError_t e = cudaSuccess;
@@ -607,7 +628,7 @@ int kda_proj_set_config(kda_plan *plan, int branch, int M, const kp_cfg *cfg) {
     const BranchShape sh = branch_shape(plan, branch);
     int rc = check_branch_cfg(branch, M, sh.N, sh.K, *cfg);
     if (rc) return rc;
-    Scratch s = scratch_of(M, sh.N, sh.K, *cfg, plan->sms);
+    Scratch s = branch_scratch(plan, branch, M, *cfg);
     if (s.floats > plan->ws_floats[branch] || s.counters > plan->cnt_n[branch])
         return set_error(KP_ETOOBIG, "kda_proj_set_config: config needs more scratch than the plan holds");
     plan->cfg[branch][M] = *cfg;

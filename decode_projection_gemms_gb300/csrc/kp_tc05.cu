@@ -14,10 +14,15 @@
 //    is the token count padded to 16 (UMMA N = 16..256), so one instruction
 //    serves every token of a 128-feature tile;
 //  * split-K over a thread-block cluster: the C CTAs of a cluster share one
-//    feature tile and each streams 1/C of its K range. Their fp32 partial
-//    tiles meet in distributed shared memory: after a cluster barrier, CTA r
-//    sums rows [r*128/C, (r+1)*128/C) of all C partials in rank order 0..C-1
-//    and rounds once to bf16. Deterministic, no global scratch, no counters;
+//    feature tile and each streams 1/C of its K range. Each writes its fp32
+//    partial tile from TMEM to a scratch area (L2-resident); after a cluster
+//    barrier, CTA r sums rows [r*128/C, (r+1)*128/C) of all C partials in rank
+//    order 0..C-1 and rounds once to bf16. Deterministic, no counters. The
+//    launches that fuse F_B keep the partial tiles in shared memory and pull
+//    them over distributed shared memory (then a second barrier keeps them
+//    alive for their readers): there the fused cluster's tail sets the
+//    launch's end, and the other CTAs leaving earlier (L2 path) let the next
+//    launch's weight stream contend with it (measured slower);
 //  * few, large TMA operations: on this part a TMA/bulk copy stream is
 //    limited by operations per issuing warp rather than by DRAM locality, so
 //    each 64-wide K block of W is one 128-row x 128-byte box (16 KB) and the
@@ -68,6 +73,9 @@ struct Tc05Params {
     __nv_bfloat16 *y2;
     int64_t ldy2;
     int *err;
+    // Split-K partial tiles (C > 1): the CTA of (token tile y, feature tile t,
+    // rank r) owns [Mpad][RT] fp32 at ws + ((y * n_tiles + t) * C + r) * Mpad * RT.
+    float *ws;
     int dtype;                 // KP_BF16 / KP_FP16: operands, output and residual
     const uint16_t *res;       // optional residual [M, ldr], added before the rounding
     int64_t ldr;
@@ -387,7 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_bounded(smem_u32(accf), 0, abort_flag, p.err, DEV_TIMEOUT_ACC_FULL);
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        float *red = reinterpret_cast<float *>(gbase);  // [Mpad][RT] fp32, reuses stage memory
+        // This CTA's partial tile [Mpad][RT] fp32 (a warp writes 32 consecutive
+        // rows, 128 bytes, per token): in the scratch area for the plain
+        // kernels, in the (by now free) stage memory for the fused-F_B one.
+        float *const red = !kFB ? p.ws + ((static_cast<size_t>(blockIdx.y) * p.n_tiles + tile) * C + rank) *
+                                             static_cast<size_t>(p.Mpad) * RT
+                                : reinterpret_cast<float *>(gbase);
         // half h of the tile: rows h*128 .. h*128+127, accumulator columns h*Mpad ..
         for (int h = 0; h < (kWide ? 2 : 1); ++h) {
             const int rt = h * kTileN + row;   // row within the tile
@@ -421,9 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (C > 1) {
-        // All partial tiles of the cluster are in shared memory after this.
+        // Every partial tile of the cluster is written (and, by the barrier's
+        // release/acquire at cluster scope, visible to every peer) after this.
         __syncwarp();
         cluster_sync_all();
+        const float *const parts = !kFB ? p.ws + (static_cast<size_t>(blockIdx.y) * p.n_tiles + tile) * C *
+                                                     static_cast<size_t>(p.Mpad) * RT
+                                        : nullptr;
+        const size_t part_stride = static_cast<size_t>(p.Mpad) * RT;   // one rank's tile
         // This CTA reduces rows r0 .. r0 + rpc - 1 of the tile for every
         // token. A thread owns four of those rows (rr .. rr + 3) and walks
         // the tokens m = t / groups, + mstep, ...: the rows and the output
@@ -501,10 +519,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < T; ++t) {
                     const int mt = m + t * mstep;
                     if (mt < Mloc) {
-                        const uint32_t off = base + static_cast<uint32_t>((mt * RT + rr) * 4);
+                        if constexpr (!kFB) {
+                            // the peers' partial tiles, through L2
+                            const float *src = parts + mt * RT + rr;
 #pragma unroll
-                        for (int c = 0; c < CM; ++c)
-                            if (c < C) part[t][c] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(c)));
+                            for (int c = 0; c < CM; ++c)
+                                if (c < C)
+                                    part[t][c] = __ldcg(reinterpret_cast<const float4 *>(src + c * part_stride));
+                        } else {
+                            // the peers' partial tiles, over distributed shared memory
+                            const uint32_t off = base + static_cast<uint32_t>((mt * RT + rr) * 4);
+#pragma unroll
+                            for (int c = 0; c < CM; ++c)
+                                if (c < C) part[t][c] = ld_dsmem_f4(mapa_shared(off, static_cast<uint32_t>(c)));
+                        }
                     }
                 }
 #pragma unroll
@@ -526,12 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             passes(std::integral_constant<int, 2>(), std::integral_constant<int, 8>());
         else
             passes(std::integral_constant<int, 1>(), std::integral_constant<int, 16>());
-        // Written F_B operand slices reach the tensor cores' (async) proxy of
-        // whichever CTA reads them after the barrier.
-        if (fused) asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-        // Peers may still be reading this CTA's partial tile; after this
-        // barrier every F_B operand slice has landed everywhere.
-        cluster_sync_all();
+        if constexpr (kFB) {
+            // Written F_B operand slices reach the tensor cores' (async) proxy
+            // of whichever CTA reads them after the barrier.
+            if (fused) asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+            // Peers may still be reading this CTA's partial tile; after this
+            // barrier every F_B operand slice has landed everywhere.
+            cluster_sync_all();
+        }
     } else if (fused) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
@@ -830,13 +860,22 @@ bool tc05_supported(int M, int N, int K, const kp_cfg &c) {
     const int ms = max_stages(Mpad, nkb, rt);
     const int st = c.stages ? c.stages : ms;
     if (st < 1 || st > ms) return false;
-    // the cluster reduction reuses the stage memory for an Mpad x rows fp32 tile
-    if (C > 1 && static_cast<size_t>(Mpad) * rt * 4 > static_cast<size_t>(st) * stage_bytes_of(Mpad, nkb, rt))
-        return false;
     return true;
 }
 
-Scratch tc05_scratch(int, int, int, const kp_cfg &, int) { return Scratch(); }
+// Split-K partial tiles: C > 1 keeps C fp32 tiles of Mpad x rows per feature
+// tile and token tile.
+Scratch tc05_scratch(int M, int N, int K, const kp_cfg &c, int) {
+    (void)K;
+    Scratch s;
+    const int C = cluster_of(c);
+    if (C == 1 || M < 1 || N < 1) return s;
+    const int rt = rows_of(c);
+    const size_t tiles = static_cast<size_t>((N + rt - 1) / rt);
+    const size_t mt = static_cast<size_t>((M + 255) / 256);
+    s.floats = mt * tiles * C * static_cast<size_t>(mpad_of(M)) * rt;
+    return s;
+}
 
 namespace {
 // Shared-memory layout of the fused F_B after the main loop (offsets from the
@@ -888,6 +927,10 @@ cudaError_t tc05_launch(const GemmArgs &a, const kp_cfg &c, int num_sms, cudaStr
         p.ldy2 = split->ldy2;
     }
     p.err = a.err;
+    p.ws = a.ws;
+    // the plain kernels' split-K partial tiles need scratch (the fused-F_B one
+    // keeps them in shared memory)
+    if (!fb && cluster_of(c) > 1 && !p.ws) return cudaErrorInvalidValue;
     p.dtype = a.dtype;
     p.res = a.res;
     p.ldr = a.ldr;

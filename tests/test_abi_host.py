@@ -145,40 +145,39 @@ def test_scratch_sizes(lib):
     one = binding.KpCfg.make("cc", split_k=1, block=256, rows=4, k_unroll=2)
     assert binding.scratch_bytes(4, 4096, 7168, one, 152) == 0
     tc = binding.KpCfg.make("tc05", split_k=4, k_unroll=2, stages=3)
-    # cluster split-K reduces in distributed shared memory: no scratch
-    assert binding.scratch_bytes(20, 4096, 7168, tc, 152) == 0
+    # cluster split-K: C fp32 partial tiles of Mpad x 128 per feature tile
+    # (M = 20 -> Mpad 32; N = 4096 -> 32 tiles)
+    assert binding.scratch_bytes(20, 4096, 7168, tc, 152) == 32 * 4 * 32 * 128 * 4
+    assert binding.scratch_bytes(20, 4096, 7168, binding.KpCfg.make("tc05", split_k=1), 152) == 0
+    # token tiles of 256 beyond M = 256: one set of partial tiles per token tile
+    tc_deep = binding.KpCfg.make("tc05", split_k=4, k_unroll=2, stages=0)
+    assert binding.scratch_bytes(300, 4096, 7168, tc_deep, 152) == 2 * 32 * 4 * 256 * 128 * 4
     for bad_tc in (binding.KpCfg.make("tc05", split_k=3), binding.KpCfg.make("tc05", split_k=32),
                    binding.KpCfg.make("tc05", k_unroll=3), binding.KpCfg.make("tc05", stages=99),
                    binding.KpCfg.make("tc05", producers=6)):
         with pytest.raises(binding.KdaProjError):
             binding.scratch_bytes(20, 4096, 7168, bad_tc, 152)
-    # 256 feature rows per CTA: the cluster reduction needs Mpad x 256 fp32
+    # 256 feature rows per CTA: partial tiles of Mpad x 256 fp32 (16 tiles)
     wide = binding.KpCfg.make("tc05", split_k=4, rows=256, k_unroll=1)
-    assert binding.scratch_bytes(64, 4096, 7168, wide, 152) == 0
-    with pytest.raises(binding.KdaProjError):
+    assert binding.scratch_bytes(64, 4096, 7168, wide, 152) == 16 * 4 * 64 * 256 * 4
+    with pytest.raises(binding.KdaProjError):   # a 256 KB stage does not fit
         binding.scratch_bytes(256, 4096, 7168, binding.KpCfg.make("tc05", split_k=4, rows=256,
-                                                                  k_unroll=2), 152)
+                                                                  k_unroll=4), 152)
     bad = binding.KpCfg.make("cc", split_k=1, block=256, rows=8, k_unroll=1)
     with pytest.raises(binding.KdaProjError) as e:
         binding.scratch_bytes(16, 4096, 7168, bad, 152)     # 8 x 16 accumulators: not built
     assert e.value.code == binding.KP_ECONFIG
 
 
-def test_partial_tile_must_fit_the_stages(lib):
-    # C > 1 reduces an Mpad x 128 fp32 partial tile in the stage memory: at
-    # M = 128 that is 64 KB, so one 32 KB stage (one K block: 16 KB W + 16 KB x)
-    # is too small and two are enough; C = 1 has no partial tile
-    def ok(M, C, stages):
-        try:
-            binding.scratch_bytes(M, 4096, 7168, binding.KpCfg.make(
-                "tc05", split_k=C, k_unroll=1, stages=stages), 152)
-            return True
-        except binding.KdaProjError as e:
-            assert e.code == binding.KP_ECONFIG
-            return False
-    assert not ok(128, 4, 1) and ok(128, 4, 2) and ok(128, 1, 1)
-    # M = 16: 8 KB partial tile, 18 KB stage
-    assert ok(16, 16, 1)
+def test_split_k_partials_need_no_stage_memory(lib):
+    # the partial tiles live in scratch, not in the pipeline's shared memory:
+    # one stage is enough for any split factor, and only split_k > 1 has scratch
+    def scratch(M, C, stages):
+        return binding.scratch_bytes(M, 4096, 7168, binding.KpCfg.make(
+            "tc05", split_k=C, k_unroll=1, stages=stages), 152)
+    assert scratch(128, 4, 1) == 32 * 4 * 128 * 128 * 4
+    assert scratch(128, 1, 1) == 0
+    assert scratch(16, 16, 1) == 32 * 16 * 16 * 128 * 4
 
 
 def test_fuse_flag_is_plan_only(lib):

@@ -375,7 +375,9 @@ def test_kda_fused_fb(plan, M, ci):
     try:
         plan.set_config(binding.BRANCH_FAB, M, cf)
     except binding.KdaProjError as e:
-        assert e.code == binding.KP_ECONFIG   # no room for the F_B operands at this M
+        # no room for the F_B operands at this M, or more split-K scratch than
+        # the plan holds
+        assert e.code in (binding.KP_ECONFIG, binding.KP_ETOOBIG)
         pytest.skip(str(e))
     x, wp, wfb = kda_inputs(M, layer=3, seed=5)
     x, wp, wfb = x.cuda(), wp.cuda(), wfb.cuda()
