@@ -123,8 +123,9 @@ typedef struct kp_cfg {
     int32_t split_k;  /* CC: number of K slices S >= 1 (S > 1 uses scratch);
                          TC05: CTAs per thread-block cluster sharing one
                          128-feature tile, each streaming 1/split_k of K
-                         (1, 2, 4, 8, 16; reduced in distributed shared
-                         memory, no scratch) */
+                         (1, 2, 4, 8, 16; with split_k > 1 each CTA's fp32
+                         partial tile goes to scratch and the cluster sums
+                         them in rank order) */
     int32_t block;    /* CC, SMALLK: threads per CTA (multiple of 32; CC <= 512,
                          SMALLK <= 256) */
     int32_t rows;     /* CC: output rows per warp (1, 2, 4, 8);
@@ -244,7 +245,10 @@ KP_API int skinny_gemm_noalloc(const void *x, const void *W, void *y, int M, int
  * rows, N_fab F_A/beta rows (the first 128 are F_A) and N_fb F_B rows, for
  * token counts 1..max_M. Picks a configuration per (branch, M) from the table,
  * and allocates (cudaMalloc, on the current device) the scratch of each branch
- * separately so the two streams never share it. The plan is immutable after
+ * separately so the two streams never share it: enough for the chosen
+ * configurations and for any tcgen05 configuration at up to 256 tokens (its
+ * split-K partial tiles: split_k * Mpad * rows fp32 per 128- or 256-row tile;
+ * about 71 MB for the Q/K/V/G branch of the pages' shapes at max_M >= 256). The plan is immutable after
  * creation except through kda_proj_set_*; it is not thread-safe to modify a
  * plan while another thread runs it.
  * Returns KP_OK, KP_EINVAL, KP_ESHAPE, KP_ENODEV or KP_ECUDA. */
