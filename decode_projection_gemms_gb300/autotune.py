@@ -143,6 +143,7 @@ class Bench:
                 b.synchronize()
                 res.append(a.elapsed_time(b) * 1e3 / (reps * self.layers))
         del g
+        _refuse_if_gave_up(cfg)
         return statistics.median(res)
 
     def bytes(self):
@@ -184,6 +185,18 @@ def sweep_candidates(M: int, N: int, K: int, sms: int):
         except binding.KdaProjError:
             pass
     return valid
+
+
+def _refuse_if_gave_up(what):
+    """After a timing run: if a kernel wait ran out during it (the error word
+    is set), report it and raise, so the candidate is dropped. Reading the word
+    clears it, so the entry points accept the next candidate's calls."""
+    torch.cuda.synchronize()
+    code = binding.device_error()
+    if code:
+        what = what.as_dict() if isinstance(what, KpCfg) else what
+        print(f"  a kernel wait ran out (code {code}) while timing {what}", file=sys.stderr)
+        raise binding.KdaProjError(binding.KP_EDEVICE, f"kernel wait ran out (code {code})")
 
 
 def sweep_shape(M, N, K, sms, device, kinds, verbose=False, quick=False):
@@ -257,6 +270,7 @@ class PlanBench:
                     b.synchronize()
                     res.append(a.elapsed_time(b) * 1e3 / (reps * self.layers))
             del g
+            _refuse_if_gave_up(f"projection M={M} mode {mode}")
             return statistics.median(res)
         finally:
             self.plan.set_overlap(-1)
@@ -283,6 +297,7 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
         if M <= 16:
             f_cands += [c for c in cc_candidates(M, pb.Nfab, pb.K, sms) if c.split_k <= 8]
         best = None
+        skipped = []
         combos = []
         for (_, cq), cf in itertools.product(q_res, f_cands):
             # a fused F_A/beta launch computes F_B itself: one F_B candidate is enough
@@ -298,6 +313,7 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
                 pb.plan.set_config(binding.BRANCH_FB, M, cb)
                 us = pb.time_call(M, 1)
             except binding.KdaProjError as e:
+                skipped.append(e)
                 if verbose:
                     print(f"  skip {cf.as_dict()}: {e}", file=sys.stderr)
                 continue
@@ -306,6 +322,11 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
                       file=sys.stderr)
             if best is None or us < best[0]:
                 best = (us, cq, cf, cb)
+        if best is None:
+            raise RuntimeError(
+                f"M={M}: no configuration combination ran ({len(q_res)} Q/K/V/G, {len(b_res)} F_B "
+                f"and {len(f_cands)} F_A/beta candidates, {len(skipped)} refused"
+                + (f"; first refusal: {skipped[0]}" if skipped else "") + ")")
         us_ovl, cq, cf, cb = best
         pb.plan.set_config(binding.BRANCH_QKVG, M, cq)
         pb.plan.set_config(binding.BRANCH_FAB, M, cf)
@@ -324,9 +345,9 @@ def tune_plan(ms, sms, device, verbose=False, top_q=3, top_b=2):
         for cand in one_cands:
             try:
                 pb.plan.set_config(binding.BRANCH_QKVG, M, cand)
+                us = pb.time_call(M, 2)
             except binding.KdaProjError:
                 continue
-            us = pb.time_call(M, 2)
             if verbose:
                 print(f"  M={M} single launch {us:8.3f} us  {cand.as_dict()}", file=sys.stderr)
             if us_one is None or us < us_one:

@@ -564,19 +564,27 @@ int kda_proj_plan(int K, int N_qkvg, int N_fab, int N_fb, int max_M, kda_plan **
             if (s.floats > need[b].floats) need[b].floats = s.floats;
             if (s.counters > need[b].counters) need[b].counters = s.counters;
         }
-        // Room for any tcgen05 configuration at up to 256 tokens (clusters of
-        // up to 16, 128 or 256 rows per CTA), so kda_proj_set_config can swap
-        // them in: the split-K partial tiles are C * Mpad * rows fp32 per tile.
+        // Room for any tcgen05 configuration at up to 256 tokens (128 or 256
+        // rows per CTA, clusters of up to 16 and at most one CTA per 64-element
+        // K block), so kda_proj_set_config can swap them in: the split-K
+        // partial tiles are C * Mpad * rows fp32 per tile.
         const int Mh = max_M < 256 ? max_M : 256;
+        int Cmax = 16;
+        while (Cmax > 1 && Cmax > (sh.K + 63) / 64) Cmax /= 2;
         for (int rows : {128, 256}) {
-            if (b == KP_BRANCH_FB) break;   // K = 128: two K blocks, no wide split
+            if (Cmax < 2) break;
             kp_cfg c = {};
             c.kind = KP_KIND_TC05;
-            c.split_k = 16;
+            c.split_k = Cmax;
             c.rows = rows;
             Scratch s = branch_scratch(p, b, Mh, c);
             if (s.floats > need[b].floats) need[b].floats = s.floats;
         }
+        // and the CUDA-core kernel's combine tickets (one per CTA row tile, at
+        // most one per output row), so a split-K CUDA-core configuration whose
+        // partials fit the space above can be swapped in too
+        const size_t rows_total = static_cast<size_t>(b == KP_BRANCH_QKVG ? p->Nq + p->Nfab : sh.N);
+        if (rows_total > need[b].counters) need[b].counters = rows_total;
     }
     cudaError_t e = cudaSuccess;
     for (int b = 0; b < 3 && e == cudaSuccess; ++b) {

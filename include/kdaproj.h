@@ -246,9 +246,12 @@ KP_API int skinny_gemm_noalloc(const void *x, const void *W, void *y, int M, int
  * token counts 1..max_M. Picks a configuration per (branch, M) from the table,
  * and allocates (cudaMalloc, on the current device) the scratch of each branch
  * separately so the two streams never share it: enough for the chosen
- * configurations and for any tcgen05 configuration at up to 256 tokens (its
- * split-K partial tiles: split_k * Mpad * rows fp32 per 128- or 256-row tile;
- * about 71 MB for the Q/K/V/G branch of the pages' shapes at max_M >= 256). The plan is immutable after
+ * configurations and, in every branch, for any tcgen05 configuration at up to
+ * 256 tokens (its split-K partial tiles: split_k * Mpad * rows fp32 per 128- or
+ * 256-row tile; about 71 MB for the Q/K/V/G branch of the pages' shapes at
+ * max_M >= 256) plus one CUDA-core combine ticket per output row (a split-K
+ * CUDA-core configuration fits when its S * M * N fp32 partials fit the space
+ * above). The plan is immutable after
  * creation except through kda_proj_set_*; it is not thread-safe to modify a
  * plan while another thread runs it.
  * Returns KP_OK, KP_EINVAL, KP_ESHAPE, KP_ENODEV or KP_ECUDA. */

@@ -589,7 +589,9 @@ def test_errors_on_device(plan):
     # a config needing more scratch than the plan holds is refused
     small = binding.KdaPlan(K=7168, N_qkvg=4096, N_fab=136, N_fb=1024, max_M=2)
     try:
-        cfg = KpCfg.make("cc", split_k=56, rows=1, k_unroll=4)
+        # 896 K slices of 8: 896 x 2 x 4232 fp32 partials, above the room for
+        # a 16-way tcgen05 split at two tokens (16 x 16 x 128 fp32 per tile)
+        cfg = KpCfg.make("cc", split_k=896, rows=1, k_unroll=4)
         with pytest.raises(binding.KdaProjError) as e:
             small.set_config(binding.BRANCH_QKVG, 2, cfg)
         assert e.value.code == binding.KP_ETOOBIG
