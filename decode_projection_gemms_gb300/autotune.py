@@ -58,10 +58,13 @@ def cc_candidates(M: int, N: int, K: int, sms: int):
                 block = 32 * warps
                 if 32 <= block <= 512 // occ:
                     out.append(KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U))
+    # each also in the shared-memory ring form (stages = 4), where it fits
+    out += [KpCfg.make("cc", split_k=c.split_k, block=c.block, rows=c.rows, k_unroll=c.k_unroll, stages=4)
+            for c in list(out)]
     # dedupe
     seen, uniq = set(), []
     for c in out:
-        key = (c.split_k, c.block, c.rows, c.k_unroll)
+        key = (c.split_k, c.block, c.rows, c.k_unroll, c.stages)
         if key not in seen:
             seen.add(key)
             uniq.append(c)
@@ -165,6 +168,15 @@ def sweep_candidates(M: int, N: int, K: int, sms: int):
             for waves in (1, 2, 4):
                 S = max(1, min(max(1, K // 256), round(waves * sms / tiles)))
                 out.append(KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U))
+        # the shared-memory ring form: 128- and 256-thread CTAs and CTAs sized
+        # so that two per SM make whole waves
+        for (R, U) in ((1, 4), (2, 2), (4, 1)) if M > 4 else ((1, 4), (2, 2)):
+            for S in (1, 2):
+                if S > max(1, K // 256):
+                    continue
+                wave = math.ceil(math.ceil(N / max(1, 2 * sms // S)) / R) * 32
+                for block in sorted({128, 256, min(512, max(32, wave))}):
+                    out.append(KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U, stages=4))
     KB = math.ceil(K / 64)
     for rows in (128, 256) if M >= 32 else (128,):
         T = math.ceil(N / rows)

@@ -26,6 +26,10 @@ SOURCES = [
     "kp_cc_inst_lo_fp16.cu",
     "kp_cc_inst_hi_fp16.cu",
     "kp_cc_inst_proj.cu",
+    "kp_cc_inst_ring_lo_bf16.cu",
+    "kp_cc_inst_ring_hi_bf16.cu",
+    "kp_cc_inst_ring_lo_fp16.cu",
+    "kp_cc_inst_ring_hi_fp16.cu",
     "kp_tc05.cu",
     "kp_smallk.cu",
     "kp_noalloc.cu",

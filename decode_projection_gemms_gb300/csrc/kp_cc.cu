@@ -10,7 +10,8 @@ namespace kp {
 
 namespace {
 
-constexpr int kMaxSmem = 200 * 1024;
+constexpr int kMaxSmem = 200 * 1024;      // x slice
+constexpr int kMaxDynSmem = 224 * 1024;   // x slice + weight ring (attribute raised to this)
 
 int cc_variant(int R, int U) {
     for (int v = 0; v < kCCVariants; ++v)
@@ -18,11 +19,25 @@ int cc_variant(int R, int U) {
     return -1;
 }
 
-CCKernelFn cc_kernel(int M, int R, int U, int dtype) {
+// stages: 0 = weights through registers, kCCRing = the shared-memory ring form.
+CCKernelFn cc_kernel(int M, int R, int U, int dtype, int stages) {
     const int v = cc_variant(R, U);
     if (v < 0 || M < 1 || M > 16 || (dtype != KP_BF16 && dtype != KP_FP16)) return nullptr;
+    if (stages == kCCRing) {
+        if (dtype == KP_FP16) return M <= 8 ? cc_ring_lo_fp16[M - 1][v] : cc_ring_hi_fp16[M - 9][v];
+        return M <= 8 ? cc_ring_lo_bf16[M - 1][v] : cc_ring_hi_bf16[M - 9][v];
+    }
+    if (stages != 0) return nullptr;
     if (dtype == KP_FP16) return M <= 8 ? cc_table_lo_fp16[M - 1][v] : cc_table_hi_fp16[M - 9][v];
     return M <= 8 ? cc_table_lo_bf16[M - 1][v] : cc_table_hi_bf16[M - 9][v];
+}
+
+// Dynamic shared memory of a launch: the x slice (16-bit), then the ring.
+size_t cc_smem_bytes(int M, int Ks, const kp_cfg &c, int *ring_off) {
+    const size_t xs = (static_cast<size_t>(M) * Ks * 2 + 15) & ~static_cast<size_t>(15);
+    if (ring_off) *ring_off = static_cast<int>(xs);
+    if (c.stages == 0) return xs;
+    return xs + cc_ring_bytes(c.block / 32, c.stages, c.rows, c.k_unroll);
 }
 
 // K slice length: ceil(K / S) rounded up to 8 elements (16 bytes).
@@ -40,7 +55,7 @@ cudaError_t ensure_smem_attr(const void *fn) {
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if (g_attr_done.count({fn, dev})) return cudaSuccess;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e == cudaSuccess) g_attr_done.insert({fn, dev});
     return e;
 }
@@ -51,9 +66,10 @@ bool cc_supported(int M, int K, const kp_cfg &c) {
     if (M < 1 || M > 16 || K < 8 || (K & 7)) return false;
     if (c.split_k < 1 || c.split_k > K / 8) return false;
     if (c.block < 32 || c.block > 512 || (c.block & 31)) return false;
-    if (!cc_kernel(M, c.rows, c.k_unroll, KP_BF16)) return false;  // same set for fp16
+    if (!cc_kernel(M, c.rows, c.k_unroll, KP_BF16, c.stages)) return false;  // same set for fp16
     const int ks = cc_slice(K, c.split_k);
-    return static_cast<long long>(M) * ks * 2 <= kMaxSmem;  // x slice (16-bit) fits in shared memory
+    if (static_cast<long long>(M) * ks * 2 > kMaxSmem) return false;  // x slice (16-bit) fits in shared memory
+    return cc_smem_bytes(M, ks, c, nullptr) <= static_cast<size_t>(kMaxDynSmem);   // and the ring beside it
 }
 
 Scratch cc_scratch(int M, int N, int K, const kp_cfg &c) {
@@ -69,7 +85,8 @@ Scratch cc_scratch(int M, int N, int K, const kp_cfg &c) {
 }
 
 bool cc_proj_supported(int M, int K, int N, const kp_cfg &c, int n_split) {
-    if (M < 1 || M > 8 || c.kind != KP_KIND_CC || c.split_k != 1 || !cc_supported(M, K, c)) return false;
+    if (M < 1 || M > 8 || c.kind != KP_KIND_CC || c.split_k != 1 || c.stages != 0 || !cc_supported(M, K, c))
+        return false;
     if (!cc_table_proj[M - 1][cc_variant(c.rows, c.k_unroll)]) return false;
     const int rows_cta = (c.block / 32) * c.rows;
     if (rows_cta > kFaWidth || kFaWidth % rows_cta) return false;   // F_A rows = whole CTAs
@@ -88,6 +105,7 @@ cudaError_t cc_proj_launch(const GemmArgs &a, const kp_cfg &c, const SplitOut &s
     p.Ks = cc_slice(a.K, 1);
     p.S = 1;
     p.rows_cta = (c.block / 32) * c.rows;
+    p.ring_off = 0;
     CCProj &q = p.proj;
     q.n_split = so.n_split;
     q.y2 = so.y2;
@@ -127,7 +145,7 @@ cudaError_t cc_proj_launch(const GemmArgs &a, const kp_cfg &c, const SplitOut &s
 
 cudaError_t cc_launch(const GemmArgs &a, const kp_cfg &c, cudaStream_t stream) {
     if (!cc_supported(a.M, a.K, c)) return cudaErrorInvalidValue;
-    CCKernelFn fn = cc_kernel(a.M, c.rows, c.k_unroll, a.dtype);
+    CCKernelFn fn = cc_kernel(a.M, c.rows, c.k_unroll, a.dtype, c.stages);
     if (!fn) return cudaErrorInvalidValue;
     CCParams p;
     p.a = a;
@@ -135,7 +153,7 @@ cudaError_t cc_launch(const GemmArgs &a, const kp_cfg &c, cudaStream_t stream) {
     p.S = (a.K + p.Ks - 1) / p.Ks;
     p.rows_cta = (c.block / 32) * c.rows;
     const int tiles = (a.N + p.rows_cta - 1) / p.rows_cta;
-    const size_t smem = static_cast<size_t>(a.M) * p.Ks * 2;   // x slice, 16-bit elements
+    const size_t smem = cc_smem_bytes(a.M, p.Ks, c, &p.ring_off);   // x slice (16-bit) + ring
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(fn));
     if (e != cudaSuccess) return e;
 

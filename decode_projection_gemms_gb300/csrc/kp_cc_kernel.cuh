@@ -16,8 +16,10 @@
 //
 // Grid: (row tiles, S). Block: `block` threads, warp w owns rows
 // tile*rows_cta + w*R .. +R-1. Lane l reads the 16-byte chunks l, l+32, ... of
-// the CTA's K slice for each of its rows; `U` chunks per row are in flight per
-// lane.
+// the CTA's K slice for each of its rows, U chunks per row at a time (a
+// batch). Two batches are in flight per lane in registers, or (NS > 0) NS - 1
+// batches in a per-warp ring in shared memory filled by asynchronous copies, so
+// the bytes in flight are not bounded by the registers.
 #pragma once
 
 #include "kp_internal.cuh"
@@ -48,8 +50,27 @@ struct CCParams {
     int Ks;       // K slice length (multiple of 8)
     int S;        // number of K slices (gridDim.y)
     int rows_cta; // output rows per CTA
+    int ring_off; // NS > 0: byte offset of the weight ring in dynamic shared memory
     CCProj proj;  // kProj kernels only
 };
+
+// Number of 16-byte chunks per lane, row and batch slot of the ring: warp w's
+// ring holds NS slots x R rows x U chunks x 32 lanes of 16 bytes.
+constexpr uint32_t cc_ring_bytes(int warps, int NS, int R, int U) {
+    return static_cast<uint32_t>(warps) * NS * R * U * 32 * 16;
+}
+
+// 16-byte asynchronous copy global -> shared (L2 policy hint), and the group
+// bookkeeping of those copies.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 constexpr int kFaWidth = 128;   // F_A columns = F_B's K
 
@@ -61,7 +82,8 @@ __device__ __forceinline__ void cc_store(const GemmArgs &a, int m, int n, float 
 }
 
 // kProj: the single-launch projection (bf16, one K slice; CCProj above).
-template <int M, int R, int U, int T, bool kProj = false>
+// NS: 0 = weights in registers (two batches); > 1 = NS-slot shared-memory ring.
+template <int M, int R, int U, int T, bool kProj = false, int NS = 0>
 // 128 registers per thread: two 256-thread CTAs or one 512-thread CTA per SM.
 __global__ void __launch_bounds__(512, 1) cc_gemv_kernel(const CCParams p) {
     extern __shared__ __align__(16) uint8_t cc_smem[];
@@ -123,7 +145,6 @@ __global__ void __launch_bounds__(512, 1) cc_gemv_kernel(const CCParams p) {
 
     // Two batches of U chunks per row in flight per warp (double buffering):
     // the next batch is requested before the current one is consumed.
-    uint4 wa[R][U], wb[R][U];
     auto load_batch = [&](uint4 (&w)[R][U], int c0) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -131,6 +152,28 @@ __global__ void __launch_bounds__(512, 1) cc_gemv_kernel(const CCParams p) {
 #pragma unroll
             for (int r = 0; r < R; ++r)
                 w[r][u] = (c < nchunk) ? ldg_stream(wrow[r] + 8 * c, pol) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    // Ring form: batch b (chunks lane + 32 * (b * U + u)) goes to slot b % NS
+    // of this warp's ring; a lane reads back only the chunks it copied, so the
+    // copies' own completion (wait_group) is the only synchronisation.
+    const int nb = (nchunk + 32 * U - 1) / (32 * U);   // batches of this lane's warp
+    const uint4 *ring = reinterpret_cast<const uint4 *>(cc_smem + p.ring_off) +
+                        static_cast<size_t>(warp) * (NS > 0 ? NS : 1) * R * U * 32 + lane;
+    auto slot = [&](int st, int r, int u) { return ((st * R + r) * U + u) * 32; };
+    auto issue = [&](int b) {
+        if constexpr (NS > 0) {
+            if (b < nb) {
+                const int st = b % NS;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int c = lane + 32 * (b * U + u);
+                    if (c < nchunk)
+#pragma unroll
+                        for (int r = 0; r < R; ++r) cp_async16(smem_u32(ring + slot(st, r, u)), wrow[r] + 8 * c, pol);
+                }
+            }
+            cp_async_commit();   // one group per batch index, empty past the end
         }
     };
 
@@ -166,7 +209,12 @@ __global__ void __launch_bounds__(512, 1) cc_gemv_kernel(const CCParams p) {
 
     // Weights never depend on the previous kernel: start streaming them
     // before waiting for it.
-    load_batch(wa, lane);
+    uint4 wa[R][U], wb[R][U];
+    if constexpr (NS > 0) {
+        for (int b = 0; b < NS - 1; ++b) issue(b);
+    } else {
+        load_batch(wa, lane);
+    }
     __syncthreads();   // the barrier's initialisation is visible to every waiter
     pdl_wait();
     pdl_trigger();
@@ -187,7 +235,7 @@ __global__ void __launch_bounds__(512, 1) cc_gemv_kernel(const CCParams p) {
         }
     }
 
-    for (int j = 0; j < iters; ++j) {
+    auto wait_x = [&](int j) {   // x piece of iteration j (kStep chunks) landed
         if (j % ipp == 0 &&
             !mbar_wait_bounded(smem_u32(&xbar[j / ipp]), 0, &abort_flag, a.err, DEV_TIMEOUT_FULL) &&
             threadIdx.x == 0) {
@@ -198,13 +246,31 @@ __global__ void __launch_bounds__(512, 1) cc_gemv_kernel(const CCParams p) {
                 while (!mbar_try_wait(smem_u32(&xbar[i]), 0) && globaltimer_ns() - t0 < 1000000000ull) {
                 }
         }
-        const int c0 = lane + j * kStep;
-        const int c1 = c0 + 32 * U;
-        const int c2 = c1 + 32 * U;
-        if (c1 < nchunk) load_batch(wb, c1);
-        compute(wa, c0);
-        if (c2 < nchunk) load_batch(wa, c2);
-        if (c1 < nchunk) compute(wb, c1);
+    };
+    if constexpr (NS > 0) {
+        for (int b = 0; b < nb; ++b) {
+            if ((b & 1) == 0) wait_x(b >> 1);
+            cp_async_wait<NS - 2>();   // this lane's batch b has landed
+            issue(b + NS - 1);         // into the slot batch b - 1 used
+            const int st = b % NS;
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int r = 0; r < R; ++r) wa[r][u] = ring[slot(st, r, u)];
+            compute(wa, lane + 32 * U * b);
+        }
+        cp_async_wait<0>();
+    } else {
+        for (int j = 0; j < iters; ++j) {
+            wait_x(j);
+            const int c0 = lane + j * kStep;
+            const int c1 = c0 + 32 * U;
+            const int c2 = c1 + 32 * U;
+            if (c1 < nchunk) load_batch(wb, c1);
+            compute(wa, c0);
+            if (c2 < nchunk) load_batch(wa, c2);
+            if (c1 < nchunk) compute(wb, c1);
+        }
     }
 
     // Butterfly reduction over the 32 lanes: every lane ends with the sums.
@@ -362,6 +428,16 @@ constexpr CCKernelFn cc_pick() {
         return nullptr;
 }
 
+// The ring form of the same kernel (a 4-slot shared-memory weight ring).
+constexpr int kCCRing = 4;
+template <int M, int V, int T>
+constexpr CCKernelFn cc_pick_ring() {
+    if constexpr (kCCR[V] * M <= 64 && (kCCR[V] < 8 || M <= 4))
+        return cc_gemv_kernel<M, kCCR[V], kCCU[V], T, false, kCCRing>;
+    else
+        return nullptr;
+}
+
 // The single-launch projection kernel for (M, variant), bf16, M <= 8.
 template <int M, int V>
 constexpr CCKernelFn cc_pick_proj() {
@@ -377,11 +453,21 @@ constexpr CCKernelFn cc_pick_proj() {
             cc_pick<M, 4, T>(), cc_pick<M, 5, T>()                                         \
     }
 
+#define KP_CC_RING_ROW(M, T)                                                                              \
+    {                                                                                                     \
+        cc_pick_ring<M, 0, T>(), cc_pick_ring<M, 1, T>(), cc_pick_ring<M, 2, T>(), cc_pick_ring<M, 3, T>(), \
+            cc_pick_ring<M, 4, T>(), cc_pick_ring<M, 5, T>()                                              \
+    }
+
 // [M - 1 within the half][variant], one table per half and element type
 extern const CCKernelFn cc_table_lo_bf16[8][kCCVariants];  // M = 1..8
 extern const CCKernelFn cc_table_hi_bf16[8][kCCVariants];  // M = 9..16
 extern const CCKernelFn cc_table_lo_fp16[8][kCCVariants];
 extern const CCKernelFn cc_table_hi_fp16[8][kCCVariants];
 extern const CCKernelFn cc_table_proj[8][kCCVariants];      // M = 1..8, bf16, kProj
+extern const CCKernelFn cc_ring_lo_bf16[8][kCCVariants];    // ring form, M = 1..8
+extern const CCKernelFn cc_ring_hi_bf16[8][kCCVariants];    // ring form, M = 9..16
+extern const CCKernelFn cc_ring_lo_fp16[8][kCCVariants];
+extern const CCKernelFn cc_ring_hi_fp16[8][kCCVariants];
 
 }  // namespace kp

@@ -132,10 +132,17 @@ typedef struct kp_cfg {
                          SMALLK: output rows per CTA (1..64);
                          TC05: feature rows per CTA, 256 (two 128-row MMAs
                          sharing each x tile) or anything else for 128 */
-    int32_t k_unroll; /* CC: 16-byte W loads in flight per row per lane (1, 2, 4);
+    int32_t k_unroll; /* CC: 16-byte W chunks per row per lane in one batch
+                         (1, 2, 4);
                          TC05: 64-wide K blocks per pipeline stage (1, 2, 4) */
     int32_t producers;/* TC05: warps issuing TMA copies per CTA (1..5; 0 = 1) */
-    int32_t stages;   /* TC05: shared-memory pipeline stages (0 = as many as fit) */
+    int32_t stages;   /* CC: 0 = two batches in flight per lane in registers;
+                         4 = each warp streams its W through a 4-slot ring in
+                         shared memory (asynchronous 16-byte copies, three
+                         batches in flight; the x slice plus block/32 * 4 *
+                         rows * k_unroll * 512 bytes of ring must fit in
+                         224 KB). Same sums, bit for bit.
+                         TC05: shared-memory pipeline stages (0 = as many as fit) */
     int32_t flags;    /* enum kp_flags */
 } kp_cfg;
 

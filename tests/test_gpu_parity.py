@@ -15,7 +15,7 @@ from decode_projection_gemms_gb300 import binding
 from decode_projection_gemms_gb300.binding import KpCfg
 from decode_projection_gemms_gb300.inputs import bf16_bits, gen_w, gen_x
 
-from gpu_helpers import (check_gemm, check_kda, gemm_case, kda_inputs,
+from gpu_helpers import (NTHREADS, check_gemm, check_kda, gemm_case, kda_inputs,
                          kda_reference, poisoned, to_f64)
 
 pytestmark = pytest.mark.gpu
@@ -83,6 +83,62 @@ def test_cc_block_sizes_and_unsplit():
     for block in (32, 128, 256, 512):
         for S in (1, 2, 16):
             check_gemm(x, W, KpCfg.make("cc", split_k=S, block=block, rows=2, k_unroll=2), "cc")
+
+
+# ---- CUDA-core kernel, shared-memory ring form (stages = 4) --------------------------------
+
+def _cc_ok(M, N, K, cfg):
+    try:
+        binding.scratch_bytes(M, N, K, cfg, 152)
+        return True
+    except binding.KdaProjError:
+        return False
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 11, 16])
+@pytest.mark.parametrize("N,K", [(136, 7168), (1000, 1024), (4096, 1032), (77, 40)])
+def test_cc_ring_shapes(M, N, K):
+    """The ring form against the oracle, and bit for bit against the register
+    form of the same configuration: both take each lane's chunks in the same
+    order, so the sums are the same."""
+    x, W = gemm_case(M, N, K, seed=M + 40)
+    ran = 0
+    for R, U in CC_VARIANTS:
+        for S, block in ((1, 256), (5, 128), (3, 448)):
+            ring = KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U, stages=4)
+            if not _cc_ok(M, N, K, ring):
+                continue
+            y, _ = check_gemm(x, W, ring, "cc ring")
+            plain = KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U)
+            y0 = binding.skinny_gemm(x.cuda(), W.cuda(), cfg=plain)
+            torch.cuda.synchronize()
+            assert torch.equal(y.view(torch.int16), y0.view(torch.int16)), (M, N, K, R, U, S, block)
+            ran += 1
+    assert ran > 0
+
+
+def test_cc_ring_full_size_qkvg():
+    """The ring form at the Q/K/V/G shape (M = 4, N = 4096, K = 7168) with
+    one K slice and 14 warps per CTA (the launch shape the benchmark times),
+    on sampled outputs."""
+    M, N, K = 4, 4096, 7168
+    x, W = gemm_case(M, N, K, seed=3)
+    cfg = KpCfg.make("cc", split_k=1, block=448, rows=2, k_unroll=2, stages=4)
+    y = binding.skinny_gemm(x.cuda(), W.cuda(), cfg=cfg)
+    torch.cuda.synchronize()
+    cols = torch.arange(0, N, 37)
+    ref = oracle.gemm(bf16_bits(x), bf16_bits(W[cols]), nthreads=NTHREADS)
+    r = oracle.compare(to_f64(y[:, cols]), ref)
+    assert r["ok"], r
+
+
+def test_cc_ring_rejects_what_does_not_fit():
+    """Only a 4-slot ring is built, and the x slice plus the ring must fit in
+    shared memory."""
+    assert not _cc_ok(4, 4096, 7168, KpCfg.make("cc", split_k=1, rows=2, k_unroll=2, stages=3))
+    # x slice 8 x 7168 x 2 = 112 KB, ring 16 warps x 4 x 4 x 2 x 512 B = 256 KB
+    assert not _cc_ok(8, 4096, 7168, KpCfg.make("cc", split_k=1, block=512, rows=4, k_unroll=2, stages=4))
+    assert _cc_ok(8, 4096, 7168, KpCfg.make("cc", split_k=2, block=256, rows=2, k_unroll=2, stages=4))
 
 
 # ---- tcgen05 kernel: token counts across the UMMA N range, ragged N and K -----------------

@@ -114,6 +114,10 @@ def _alternatives(M, N, K, pick):
             tiles = math.ceil(N / (block // 32 * R))
             S = max(1, min(max(1, K // 256), round(sms / tiles)))
             out.append(KpCfg.make("cc", split_k=S, block=block, rows=R, k_unroll=U))
+        # the shared-memory ring form, one K slice and two, 128-thread CTAs
+        for (R, U) in ((1, 4), (2, 2)):
+            for S in (1, 2):
+                out.append(KpCfg.make("cc", split_k=S, block=128, rows=R, k_unroll=U, stages=4))
     if K <= 256:
         out.append(KpCfg.make("smallk", block=256, rows=16))
     if pick.kind == binding.KIND_TC05:
