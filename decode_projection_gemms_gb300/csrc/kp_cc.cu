@@ -11,7 +11,8 @@ namespace kp {
 namespace {
 
 constexpr int kMaxSmem = 200 * 1024;      // x slice
-constexpr int kMaxDynSmem = 224 * 1024;   // x slice + weight ring (attribute raised to this)
+constexpr int kMaxDynSmem = 220 * 1024;   // x slice + weight ring (attribute raised to this; it
+                                          // leaves room for the static shared memory)
 
 int cc_variant(int R, int U) {
     for (int v = 0; v < kCCVariants; ++v)

@@ -141,7 +141,7 @@ typedef struct kp_cfg {
                          shared memory (asynchronous 16-byte copies, three
                          batches in flight; the x slice plus block/32 * 4 *
                          rows * k_unroll * 512 bytes of ring must fit in
-                         224 KB). Same sums, bit for bit.
+                         220 KB). Same sums, bit for bit.
                          TC05: shared-memory pipeline stages (0 = as many as fit) */
     int32_t flags;    /* enum kp_flags */
 } kp_cfg;
