@@ -46,7 +46,10 @@ def sampled_check(y, x_bits, w_bits, label, dtype="bf16", res_bits=None, seed=0)
     assert c["ok"], f"{label} ({len(cols)} columns): {c}"
 
 
-CONFIGS = [None, KpCfg.make("tc05", split_k=1, k_unroll=1), KpCfg.make("tc05", split_k=4, k_unroll=2, stages=2)]
+CONFIGS = [None, KpCfg.make("tc05", split_k=1, k_unroll=1), KpCfg.make("tc05", split_k=4, k_unroll=2, stages=2),
+           # 256-row CTAs with cluster split-K (the table's M = 512 and 1024 prefill entries)
+           KpCfg.make("tc05", split_k=4, rows=256, k_unroll=1),
+           KpCfg.make("tc05", split_k=2, rows=256, k_unroll=1, stages=3)]
 
 
 @pytest.mark.parametrize("M", [257, 300, 513, 1024])
