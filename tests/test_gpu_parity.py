@@ -617,6 +617,24 @@ def test_single_launch_falls_back_for_a_cuda_core_config(plan):
         plan.set_overlap(-1)
 
 
+def test_plan_takes_any_split_within_its_reserve():
+    """A plan reserves scratch for every tcgen05 split its branches' K allows
+    at up to 256 tokens (F_B's K = 128: two K blocks, so a split of 2) and a
+    combine ticket per output row, whatever its table entries need: a small
+    plan accepts a 2-way tcgen05 F_B and a split-K CUDA-core Q/K/V/G
+    configuration whose partials fit, and computes with them."""
+    M = 4
+    p = binding.KdaPlan(K=7168, N_qkvg=4096, N_fab=136, N_fb=1024, max_M=M)
+    try:
+        p.set_config(binding.BRANCH_FB, M, KpCfg.make("tc05", split_k=2, k_unroll=1))
+        p.set_config(binding.BRANCH_QKVG, M, KpCfg.make("cc", split_k=4, block=256, rows=2, k_unroll=4))
+        x, wp, wfb = kda_inputs(M, layer=3, seed=12)
+        outs = _run_mode(p, x.cuda(), wp.cuda(), wfb.cuda(), 0, torch.cuda.Stream(), binding.make_events())
+        check_kda(outs, x, wp, wfb, 4096, 136, "reserve-sized configs")
+    finally:
+        p.close()
+
+
 # ---- boundary errors on a live device -------------------------------------------------------
 
 def test_errors_on_device(plan):
