@@ -127,6 +127,27 @@ def test_table_lookup_rounds_m_up(lib, tmp_path):
         binding.table_load()
 
 
+def test_shipped_table_entries_are_valid(lib):
+    """Every entry of the shipped table names a configuration the library
+    accepts for its shape (kernel built, shared memory and cluster limits),
+    so no lookup hands a kernel a configuration it refuses. Entries with
+    KP_FLAG_FUSE_FB belong to a plan's F_A/beta branch and are checked
+    without the flag (the plan checks the fused form when it loads them)."""
+    binding.table_load()
+    assert binding.table_size() > 0
+    n = 0
+    for line in open(binding.TABLE_PATH):
+        f = line.split("#")[0].split()
+        if len(f) < 12:
+            continue
+        M, N, K = (int(v) for v in f[:3])
+        cfg = binding.KpCfg.make(f[3], *(int(v) for v in f[4:11]))
+        cfg.flags &= ~binding.FLAG_FUSE_FB
+        binding.scratch_bytes(M, N, K, cfg, 152)   # raises KP_ECONFIG if refused
+        n += 1
+    assert n == binding.table_size()
+
+
 def test_table_rejects_malformed(lib, tmp_path):
     t = tmp_path / "bad.txt"
     t.write_text("1 4096 7168 cc 7 256\n")
