@@ -1,11 +1,10 @@
 // skinny_gemm_noalloc: the CUDA-core split-K GEMM with its scratch in a fixed
 // device array that the library carries, for callers that must not allocate.
 //
-// Who needs this: code that runs while a CUDA graph is being captured (a
-// cudaMalloc there is illegal and breaks the capture), processes whose device
-// memory is owned by a pooling/caching allocator that forbids the CUDA
-// runtime from taking memory behind its back, and latency-critical paths that
-// cannot afford cudaMalloc's implicit device synchronisation. skinny_gemm grows
+// Who needs this: processes whose device memory is owned by a pooling/caching
+// allocator that forbids the CUDA runtime from taking memory behind its back,
+// and latency-critical paths that cannot afford cudaMalloc's implicit device
+// synchronisation. skinny_gemm grows
 // a workspace on demand; this entry point never does.
 //
 // The scratch is a file-scope __device__ array: every GPU that loads the

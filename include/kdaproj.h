@@ -208,10 +208,9 @@ KP_API int kp_table_size(void);
  * library itself carries, so the call never allocates. (The pages have no
  * counterpart: this entry point exists for callers of this library.)
  *
- * Meant for callers that cannot call cudaMalloc: code running inside CUDA
- * graph capture, processes whose device memory is managed by a pooling
- * allocator, and latency-critical paths that cannot take cudaMalloc's device
- * synchronisation. The caller still passes x, W and y (same layout as
+ * Meant for callers that cannot call cudaMalloc: processes whose device
+ * memory is managed by a pooling allocator, and latency-critical paths that
+ * cannot take cudaMalloc's device synchronisation. The caller still passes x, W and y (same layout as
  * skinny_gemm); the call calls no cudaMalloc, cudaFree or allocating library
  * routine.
  *   - Limits: M <= 16 (CUDA-core kernel). The kernel stages x's K slice in
@@ -234,11 +233,10 @@ KP_API int kp_table_size(void);
  *     (2 MiB + 32 KiB) until the process exits.
  *   - First call per device: looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); it allocates and
- *     synchronises nothing, but make that first call before any stream
- *     capture. Later calls only launch the kernel.
+ *     synchronises nothing. Later calls only launch the kernel.
  *   - Sharing: all calls on a device use the same array and it keeps the last
- *     call's partial sums; calls that overlap on the GPU (different streams,
- *     or concurrent graph branches) race and give wrong results. Serialise
+ *     call's partial sums; calls that overlap on the GPU (for example on
+ *     different streams) race and give wrong results. Serialise
  *     them.
  * Returns KP_OK, KP_EINVAL, KP_EALIGN, KP_ESHAPE, KP_ECONFIG, KP_ETOOBIG,
  * KP_ENODEV, KP_ECUDA. */

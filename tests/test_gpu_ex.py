@@ -55,6 +55,9 @@ def check_ex(x, W, r, dtype, cfg, label=""):
 CONFIGS = {
     "cc_split4": KpCfg.make("cc", split_k=4, block=256, rows=2, k_unroll=2),
     "cc_split1": KpCfg.make("cc", split_k=1, block=128, rows=1, k_unroll=4),
+    # the shared-memory ring form, one K slice and three
+    "cc_ring_split1": KpCfg.make("cc", split_k=1, block=256, rows=2, k_unroll=2, stages=4),
+    "cc_ring_split3": KpCfg.make("cc", split_k=3, block=128, rows=4, k_unroll=1, stages=4),
     "tc05_c1": KpCfg.make("tc05", split_k=1, k_unroll=2),
     "tc05_c4": KpCfg.make("tc05", split_k=4, k_unroll=2, stages=3),
     "tc05_c16": KpCfg.make("tc05", split_k=16, k_unroll=1),

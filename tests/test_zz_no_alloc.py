@@ -1,9 +1,9 @@
 """skinny_gemm_noalloc, called through the C ABI, must give what skinny_gemm
 gives for the same inputs, on two calls in a row.
 
-skinny_gemm_noalloc is for callers that cannot allocate device memory (code
-running under CUDA graph capture, processes whose memory belongs to a pooling
-allocator, paths that cannot take cudaMalloc's synchronisation): its split-K
+skinny_gemm_noalloc is for callers that cannot allocate device memory
+(processes whose memory belongs to a pooling allocator, paths that cannot take
+cudaMalloc's synchronisation): its split-K
 partial sums live in a fixed device array inside the library. The second call
 checks that the shared array (tickets left at zero, partial sums overwritten)
 serves a new call correctly. This file sorts last so a run that stops at the
