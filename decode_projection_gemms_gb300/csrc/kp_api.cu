@@ -59,11 +59,14 @@ struct DevState {
     // refuse new work after a give-up without synchronising.
     int *err = nullptr;
     int *err_host = nullptr;
-    // skinny_gemm's scratch, grown on demand
+    // skinny_gemm's scratch, grown on demand. A buffer that growth replaces is
+    // kept (never freed while the process runs): work captured into a CUDA
+    // graph before the growth still points at it.
     float *ws = nullptr;
     size_t ws_floats = 0;
     int *cnt = nullptr;
     size_t cnt_n = 0;
+    std::vector<void *> retired;
 };
 
 static std::mutex g_dev_mu;
@@ -479,7 +482,7 @@ int skinny_gemm_ex(const void *x, const void *W, const void *residual, void *y, 
             size_t nf = need.floats > d->ws_floats ? need.floats : d->ws_floats;
             size_t nc = need.counters > d->cnt_n ? need.counters : d->cnt_n;
             if (nf > d->ws_floats) {
-                if (d->ws) cudaFree(d->ws);
+                if (d->ws) d->retired.push_back(d->ws);
                 d->ws = nullptr;
                 d->ws_floats = 0;
                 if ((e = cudaMalloc(&d->ws, nf * sizeof(float))) != cudaSuccess)
@@ -487,7 +490,7 @@ int skinny_gemm_ex(const void *x, const void *W, const void *residual, void *y, 
                 d->ws_floats = nf;
             }
             if (nc > d->cnt_n) {
-                if (d->cnt) cudaFree(d->cnt);
+                if (d->cnt) d->retired.push_back(d->cnt);   // its tickets are all zero
                 d->cnt = nullptr;
                 d->cnt_n = 0;
                 if ((e = cudaMalloc(&d->cnt, nc * sizeof(int))) != cudaSuccess)

@@ -81,11 +81,23 @@ __device__ __forceinline__ void cc_store(const GemmArgs &a, int m, int n, float 
     reinterpret_cast<uint16_t *>(a.y)[m * a.ldy + n] = elem_round<T>(v);
 }
 
+// CTAs per SM the kernel is compiled for. The single-launch form's F_B code
+// needs registers the plain kernel does not. Where the main loop fits in 64
+// registers, this form also asks for two 512-thread CTAs per SM (64 registers
+// each, the F_B part may spill), as the plain kernel gets by itself. With one
+// CTA per SM, a 16-row, 512-thread configuration at M = 1 took 20.7 instead of
+// 11.8 us per call.
+template <int M, int R, int U, int NS, bool kProj>
+constexpr int cc_min_blocks() {
+    return kProj && (NS > 0 ? 1 : 2) * R * U * 4 + R * M + 24 <= 60 ? 2 : 1;
+}
+
 // kProj: the single-launch projection (bf16, one K slice; CCProj above).
 // NS: 0 = weights in registers (two batches); > 1 = NS-slot shared-memory ring.
 template <int M, int R, int U, int T, bool kProj = false, int NS = 0>
-// 128 registers per thread: two 256-thread CTAs or one 512-thread CTA per SM.
-__global__ void __launch_bounds__(512, 1) cc_gemv_kernel(const CCParams p) {
+// At most 128 registers per thread: two 256-thread CTAs or one 512-thread CTA
+// per SM (64 and two 512-thread CTAs for the small single-launch forms).
+__global__ void __launch_bounds__(512, (cc_min_blocks<M, R, U, NS, kProj>())) cc_gemv_kernel(const CCParams p) {
     extern __shared__ __align__(16) uint8_t cc_smem[];
     const uint16_t *xs = reinterpret_cast<const uint16_t *>(cc_smem);  // [M][Ks], 16-bit
     // x's slice lands in up to kXPieces K ranges, each on its own barrier, so

@@ -161,9 +161,12 @@ typedef struct kda_plan kda_plan;
  * tile while it is in L2 (the CUDA-core kernel takes M <= 16).
  * Scratch: split-K partial sums and tile counters live in a per-device
  * workspace owned by the library. It grows on demand, so the first call of a
- * larger shape may allocate (cudaMalloc); do one call per shape before stream
- * capture. Calls that use this workspace must not run concurrently on one
- * device (use one stream, or kda_proj_* whose plans own their scratch).
+ * larger shape may allocate (cudaMalloc, with a device synchronisation); do
+ * one call per shape before stream capture. A workspace that growth replaces
+ * stays allocated until the process exits, so work captured into a CUDA graph
+ * before a later growth keeps valid scratch. Calls that use this workspace
+ * must not run concurrently on one device (use one stream, or kda_proj_*
+ * whose plans own their scratch).
  * Returns KP_OK, KP_EINVAL, KP_EALIGN, KP_ESHAPE, KP_ECONFIG, KP_ENODEV,
  * KP_ECUDA. */
 KP_API int skinny_gemm(const void *x, const void *W, void *y, int M, int N, int K,

@@ -682,3 +682,29 @@ def test_repeat_calls_bit_identical():
         b = binding.skinny_gemm(x, W, cfg=cfg)
         torch.cuda.synchronize()
         assert torch.equal(a, b)
+
+
+def test_graph_keeps_its_scratch_after_the_workspace_grows():
+    """skinny_gemm's per-device workspace grows on demand; the buffer it
+    replaces stays allocated, so a graph captured before the growth still
+    computes the same outputs when replayed after it."""
+    M, N, K = 4, 4096, 7168
+    x, W = gemm_case(M, N, K, seed=21)
+    x, W = x.cuda(), W.cuda()
+    cfg = KpCfg.make("tc05", split_k=8, k_unroll=2)   # partial tiles in the workspace
+    ref = binding.skinny_gemm(x, W, cfg=cfg)
+    torch.cuda.synchronize()
+    y = poisoned((M, N))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.skinny_gemm(x, W, y, cfg=cfg)
+    # 448 K slices x 16 tokens x 16384 rows of fp32 partial sums (470 MB):
+    # more than any call before it needs, so the workspace grows
+    xb = torch.zeros((16, K), dtype=torch.bfloat16, device="cuda")
+    Wb = torch.zeros((16384, K), dtype=torch.bfloat16, device="cuda")
+    binding.skinny_gemm(xb, Wb, cfg=KpCfg.make("cc", split_k=448, block=256, rows=4, k_unroll=1))
+    torch.cuda.synchronize()
+    del xb, Wb
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)
