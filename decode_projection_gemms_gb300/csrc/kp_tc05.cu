@@ -28,7 +28,7 @@
 //    each 64-wide K block of W is one 128-row x 128-byte box (16 KB) and the
 //    x operand of a whole stage (nkb K blocks) is one 3-D box; stages are kept
 //    small enough for two CTAs per SM, whose producers stream concurrently;
-//  * cta_group::1, no multicast.
+//  * cta_group::1; every CTA loads its own operand tiles.
 //
 // Warp roles (192 threads): warp 1 = TMEM allocator + MMA issuer (one lane),
 // warps 2..5 = epilogue (TMEM lane quarter = warp % 4). TMA copies are issued
