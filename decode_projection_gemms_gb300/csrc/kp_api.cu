@@ -479,8 +479,11 @@ int skinny_gemm_ex(const void *x, const void *W, const void *residual, void *y, 
             // Grow (rare; never during capture if the caller warmed up).
             cudaError_t e = cudaDeviceSynchronize();
             if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-            size_t nf = need.floats > d->ws_floats ? need.floats : d->ws_floats;
-            size_t nc = need.counters > d->cnt_n ? need.counters : d->cnt_n;
+            // At least double what is there, so that the replaced buffers
+            // (kept, see DevState) add up to less than the final one.
+            size_t nf = d->ws_floats, nc = d->cnt_n;
+            if (need.floats > nf) nf = need.floats > 2 * nf ? need.floats : 2 * nf;
+            if (need.counters > nc) nc = need.counters > 2 * nc ? need.counters : 2 * nc;
             if (nf > d->ws_floats) {
                 if (d->ws) d->retired.push_back(d->ws);
                 d->ws = nullptr;

@@ -164,7 +164,8 @@ typedef struct kda_plan kda_plan;
  * larger shape may allocate (cudaMalloc, with a device synchronisation); do
  * one call per shape before stream capture. A workspace that growth replaces
  * stays allocated until the process exits, so work captured into a CUDA graph
- * before a later growth keeps valid scratch. Calls that use this workspace
+ * before a later growth keeps valid scratch; each growth at least doubles the
+ * workspace, so the kept buffers add up to less than the current one. Calls that use this workspace
  * must not run concurrently on one device (use one stream, or kda_proj_*
  * whose plans own their scratch).
  * Returns KP_OK, KP_EINVAL, KP_EALIGN, KP_ESHAPE, KP_ECONFIG, KP_ENODEV,
