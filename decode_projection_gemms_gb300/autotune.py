@@ -156,7 +156,8 @@ class Bench:
 def sweep_candidates(M: int, N: int, K: int, sms: int):
     """A short list for the shape sweep: the settings that decided the
     projection shapes' tuning (grids of one to two CTAs per SM, split-K to fill
-    them, two K blocks per stage, as many stages as fit), around 10 per shape."""
+    them, two K blocks per stage, as many stages as fit), 10 to 30 per shape
+    (the CUDA-core kernel's ring form adds up to 17 at M <= 16)."""
     out = []
     if K <= 256:
         out += [KpCfg.make("smallk", block=256, rows=r) for r in (8, 16)]
